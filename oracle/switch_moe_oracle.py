@@ -1,0 +1,291 @@
+"""Plain fp64 CPU oracle of the Switch top-1 MoE layer forward.
+
+TEST INFRASTRUCTURE.  Only tests, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this module.  It shares no code,
+header, table or helper with the CUDA library and never calls it.
+
+Every step is the plain definition from the pages, one step after another,
+in float64 (inputs are the exact bf16 / fp32 values widened to float64).
+A library primitive (matmul, argmax, exp) serves as a step; there is no
+blocking, fusion or reordering beyond the definitions.
+
+Sources (page title, then section / equation / figure):
+
+* [TOP1]  "Top-1 路由 (Top-1 Routing)", compassingai.com -- core mechanism
+  steps 1-3 (gating softmax, top-1 argmax and gate value, expert output),
+  load-balancing section (auxiliary loss), Token Dropping section
+  (capacity per expert), key-parameter section (two-layer FFN, no bias).
+* [SWITCH] Switch Transformer walk-through, personwebsite.pages.dev/moe-switch
+  -- Switch layer (gate value as the multiplier, Eq. 2), expert capacity
+  (dropped tokens skip the expert and ride the residual), load-balancing
+  loss (Eq. 4, whose symbols f_i and P_i survive in the text), selective
+  float32 router precision.
+* [CAP]   "MoE 专家容量因子与 Token 丢弃", wiblog.cn -- capacity formula
+  (section on where capacity comes from), overflow handling (section on
+  what happens after overflow: sort by routing weight, keep the highest),
+  the token-path flowchart (nodes D -> F: the capacity decision is taken
+  after all scores are known and before any expert runs).
+* [CMP]   "Which Routing Does Each MoE Model Use?" (MarkTechPost digest) --
+  routing table: Llama 4 Maverick routes top-1 over 128 experts plus one
+  always-on shared expert.
+
+Readings where the pages are silent or disagree (each is a choice, made
+once, and stated here):
+
+* capacity rounds up: C = ceil(cf * T / N), evaluated in double as
+  (cf * T) / N; C must be >= 1.
+* argmax is taken on the logits (same order as on the softmax scores), and
+  the lowest expert index wins exact ties.
+* f_i counts the router's choices before capacity (tokens *routed* to i).
+* gate-value priority orders an expert's tokens by (gate desc, token asc);
+  the slot of a kept token is its rank in that order.  Token-order priority
+  gives slot = number of earlier tokens with the same expert.
+* a dropped token's MoE output is the zero vector; the caller adds the
+  residual.  The shared expert (when present) runs on every token,
+  dropped or not.
+* the expert FFN is ReLU between two bias-free linear maps.
+* whether the gate scales the expert output is a flag (TOP1 says Switch
+  does not scale; SWITCH Eq. 2 says the gate is the multiplier).
+"""
+from __future__ import annotations
+
+import math
+from typing import Callable, Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "TOKEN_ORDER", "GATE_PRIORITY",
+    "capacity", "router_logits", "softmax", "top1", "route", "route_from_logits",
+    "assign_slots", "expert_ffn", "aux_loss", "combine_token", "forward",
+    "forward_rows",
+]
+
+TOKEN_ORDER = 0
+GATE_PRIORITY = 1
+
+
+def _f64(a) -> np.ndarray:
+    """Widen a numpy array or a (CPU) torch tensor of any float dtype to float64."""
+    if hasattr(a, "detach"):  # torch tensor; bf16 has no numpy dtype
+        a = a.detach().to("cpu")
+        import torch  # local: numpy-only callers never need torch
+        a = a.to(torch.float64).numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Step a3: expert capacity.
+#   [TOP1] Token Dropping section; [CAP] section on where capacity comes
+#   from: capacity = capacity_factor * tokens_per_batch / num_experts.
+#   Rounding is not on the pages: ceil, in double, in this evaluation order.
+# --------------------------------------------------------------------------
+def capacity(T: int, N: int, capacity_factor: float) -> int:
+    if T <= 0 or N <= 0 or not (capacity_factor > 0) or math.isinf(capacity_factor):
+        raise ValueError("capacity needs T > 0, N > 0 and a finite cf > 0")
+    c = math.ceil(float(capacity_factor) * float(T) / float(N))
+    if c < 1:
+        raise ValueError("capacity rounds to zero")
+    return int(c)
+
+
+# --------------------------------------------------------------------------
+# Step a1: router logits h = W_g . x  ([TOP1] core mechanism step 1,
+# W_g in R^{N x d}; [SWITCH] router variable producing logits).  The
+# optional per-expert bias b_g only serves to skew a synthetic workload.
+# --------------------------------------------------------------------------
+def router_logits(x, W_g, b_g=None) -> np.ndarray:
+    x64 = _f64(x)
+    W64 = _f64(W_g)
+    logits = x64 @ W64.T                      # [T, N]
+    if b_g is not None:
+        logits = logits + _f64(b_g)[None, :]
+    return logits
+
+
+# Step a2: score = softmax(logits) over the N experts ([TOP1] step 1).
+def softmax(logits) -> np.ndarray:
+    l = _f64(logits)
+    m = l.max(axis=1, keepdims=True)
+    ex = np.exp(l - m)
+    return ex / ex.sum(axis=1, keepdims=True)
+
+
+# Step a2: expert_id = argmax(score), gate_value = score[expert_id]
+# ([TOP1] step 2).  Argmax on the logits; the lowest index wins ties.
+def top1(logits, probs):
+    l = _f64(logits)
+    p = _f64(probs)
+    T = l.shape[0]
+    expert_id = np.empty(T, dtype=np.int64)
+    for t in range(T):
+        row = l[t]
+        best = 0
+        for i in range(1, row.shape[0]):
+            if row[i] > row[best]:           # strict: an equal later logit never wins
+                best = i
+        expert_id[t] = best
+    gate = p[np.arange(T), expert_id]
+    return expert_id, gate
+
+
+def _top1_fast(l: np.ndarray, p: np.ndarray):
+    # np.argmax returns the first maximal index, the same rule as top1();
+    # used for large T where the per-token Python loop is too slow.
+    e = np.argmax(l, axis=1).astype(np.int64)
+    return e, p[np.arange(l.shape[0]), e]
+
+
+def route(x, W_g, b_g=None):
+    """Router of one batch: logits, probabilities, expert_id, gate (fp64)."""
+    l = router_logits(x, W_g, b_g)
+    p = softmax(l)
+    e, g = (_top1_fast(l, p) if l.shape[0] > 4096 else top1(l, p))
+    return {"logits": l, "probs": p, "expert_id": e, "gate": g}
+
+
+def route_from_logits(logits32):
+    """Routing decisions on given (fp32) logits; the comparisons that pick
+    the expert see exactly those values (fp32 values are exact in fp64)."""
+    l = _f64(logits32)
+    p = softmax(l)
+    e, g = (_top1_fast(l, p) if l.shape[0] > 4096 else top1(l, p))
+    return {"logits": l, "probs": p, "expert_id": e, "gate": g}
+
+
+# --------------------------------------------------------------------------
+# Steps a4 / a4': slot assignment and overflow.
+#   [SWITCH] expert capacity: tokens beyond an expert's capacity are dropped.
+#   [CAP] overflow section + flowchart D -> F: sort an expert's tokens by
+#   routing weight, keep the highest-weight ones, mark the rest overflow;
+#   decided after all scores are known, before any expert computes.
+# --------------------------------------------------------------------------
+def assign_slots(expert_id, gate, N: int, C: int, priority_mode: int = TOKEN_ORDER):
+    """Returns (slot int64[T] with -1 for dropped, drop uint8[T],
+    counts int64[N] = tokens routed to each expert before capacity)."""
+    e = np.asarray(expert_id, dtype=np.int64)
+    T = e.shape[0]
+    slot = np.full(T, -1, dtype=np.int64)
+    counts = np.zeros(N, dtype=np.int64)
+    if priority_mode == TOKEN_ORDER:
+        for t in range(T):                    # a stable pass in token order
+            pos = counts[e[t]]
+            counts[e[t]] += 1
+            if pos < C:
+                slot[t] = pos
+    elif priority_mode == GATE_PRIORITY:
+        g = np.asarray(gate, dtype=np.float64)
+        members = [[] for _ in range(N)]
+        for t in range(T):
+            members[e[t]].append(t)
+        for i in range(N):
+            counts[i] = len(members[i])
+            order = sorted(members[i], key=lambda t: (-g[t], t))
+            for rank, t in enumerate(order):
+                if rank < C:
+                    slot[t] = rank
+    else:
+        raise ValueError("priority_mode must be 0 (token order) or 1 (gate priority)")
+    drop = (slot < 0).astype(np.uint8)
+    return slot, drop, counts
+
+
+# --------------------------------------------------------------------------
+# Step a6/a7: the expert, a two-layer bias-free FFN ([TOP1] key-parameter
+# section: about 2 * d_model * d_ff weights per expert).  ReLU between.
+#   W1_e: [d_ff, d_model], W2_e: [d_model, d_ff] (out-features first).
+# --------------------------------------------------------------------------
+def expert_ffn(x_rows, W1_e, W2_e) -> np.ndarray:
+    xr = _f64(x_rows)
+    h = xr @ _f64(W1_e).T                      # [n, d_ff]
+    h = np.maximum(h, 0.0)
+    return h @ _f64(W2_e).T                    # [n, d_model]
+
+
+# --------------------------------------------------------------------------
+# Step a10: L_aux = N * sum_i f_i * P_i  ([TOP1] load-balancing section;
+# [SWITCH] Eq. 4 text): f_i = share of the batch's tokens routed to expert i,
+# P_i = mean router probability of expert i over the batch.  Unscaled by
+# the coefficient alpha (the caller applies it).
+# --------------------------------------------------------------------------
+def aux_loss(probs, counts) -> float:
+    p = _f64(probs)
+    T, N = p.shape
+    f = np.asarray(counts, dtype=np.float64) / T
+    P = p.sum(axis=0) / T
+    return float(N * np.sum(f * P))
+
+
+# Step a9: combine one token.  [TOP1] step 3 / [SWITCH] Eq. 2 (gate flag);
+# [SWITCH] capacity section and [CAP] overflow section: a dropped token gets
+# no expert output (zero vector; the residual is the caller's).
+def combine_token(o_row: Optional[np.ndarray], gate: float, dropped: bool,
+                  gate_multiply: bool, d_model: int,
+                  shared_row: Optional[np.ndarray] = None) -> np.ndarray:
+    if dropped:
+        y = np.zeros(d_model, dtype=np.float64)
+    else:
+        y = (gate if gate_multiply else 1.0) * o_row
+    if shared_row is not None:                 # [CMP]: shared expert is always on
+        y = y + shared_row
+    return y
+
+
+def forward(x, W_g, W1, W2, capacity_factor: float, priority_mode: int = TOKEN_ORDER,
+            gate_multiply: int = 1, b_g=None, W1s=None, W2s=None,
+            expert_getter: Optional[Callable[[int], tuple]] = None):
+    """The whole layer on one batch.
+
+    W1 / W2 are [N, F, d] / [N, d, F]; alternatively ``expert_getter(e)``
+    returns (W1_e, W2_e) so that large layers need not be held whole.
+    Returns a dict with y (fp64 [T, d]), routing outputs and aux_loss."""
+    r = route(x, W_g, b_g)
+    T, N = r["probs"].shape
+    C = capacity(T, N, capacity_factor)
+    slot, drop, counts = assign_slots(r["expert_id"], r["gate"], N, C, priority_mode)
+    d = x.shape[1]
+    y = np.zeros((T, d), dtype=np.float64)
+    o = np.zeros((T, d), dtype=np.float64)
+    for i in range(N):
+        rows = np.nonzero((r["expert_id"] == i) & (slot >= 0))[0]
+        if rows.size == 0:
+            continue
+        W1_e, W2_e = expert_getter(i) if expert_getter else (W1[i], W2[i])
+        o[rows] = expert_ffn(_rows(x, rows), W1_e, W2_e)
+    S = expert_ffn(x, W1s, W2s) if W1s is not None else None
+    for t in range(T):
+        y[t] = combine_token(o[t], r["gate"][t], bool(drop[t]), bool(gate_multiply), d,
+                             None if S is None else S[t])
+    return {"y": y, "expert_id": r["expert_id"], "gate": r["gate"], "slot": slot,
+            "drop": drop, "counts": counts, "aux_loss": aux_loss(r["probs"], counts),
+            "logits": r["logits"], "probs": r["probs"], "capacity": C}
+
+
+def forward_rows(rows: Sequence[int], x, expert_id, gate, slot, gate_multiply: int,
+                 expert_getter: Callable[[int], tuple], W1s=None, W2s=None) -> np.ndarray:
+    """y for a sample of tokens, given routing decisions (for layers too large
+    to run whole): rows are grouped by expert so each expert is fetched once."""
+    rows = np.asarray(rows, dtype=np.int64)
+    d = x.shape[1]
+    out = np.zeros((rows.size, d), dtype=np.float64)
+    e = np.asarray(expert_id)[rows]
+    s = np.asarray(slot)[rows]
+    g = np.asarray(gate, dtype=np.float64)[rows]
+    xr = _rows(x, rows)
+    o = np.zeros((rows.size, d), dtype=np.float64)
+    for i in np.unique(e[s >= 0]):
+        sel = np.nonzero((e == i) & (s >= 0))[0]
+        W1_e, W2_e = expert_getter(int(i))
+        o[sel] = expert_ffn(xr[sel], W1_e, W2_e)
+    S = expert_ffn(xr, W1s, W2s) if W1s is not None else None
+    for k in range(rows.size):
+        out[k] = combine_token(o[k], g[k], bool(s[k] < 0), bool(gate_multiply), d,
+                               None if S is None else S[k])
+    return out
+
+
+def _rows(x, rows):
+    if hasattr(x, "detach"):
+        import torch
+        return _f64(x[torch.as_tensor(rows, dtype=torch.long, device=x.device)])
+    return _f64(x)[rows]

@@ -1,0 +1,408 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test ties one oracle function to something other than itself: a value
+worked by hand from the pages' formulas (tests/golden/), a closed form, a
+brute-force definition on tiny inputs, an invariant, or a library routine
+that computes the same special case.  They run without a GPU.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from oracle import switch_moe_oracle as OM
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- capacity
+def _golden_capacity():
+    rows = []
+    with open(os.path.join(GOLDEN, "capacity.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                T, N, cf, C = line.split()
+                rows.append((int(T), int(N), float(cf), int(C)))
+    return rows
+
+
+@pytest.mark.parametrize("T,N,cf,C", _golden_capacity())
+def test_capacity_golden(T, N, cf, C):
+    assert O.capacity(T, N, cf) == C
+
+
+def test_capacity_properties():
+    rng = np.random.default_rng(0)
+    for _ in range(2000):
+        T = int(rng.integers(1, 100000))
+        N = int(rng.integers(1, 512))
+        cf = float(rng.uniform(0.05, 4.0))
+        C = O.capacity(T, N, cf)
+        # C is the least integer with C >= cf*T/N (checked in exact rationals
+        # for the double value of cf)
+        from fractions import Fraction
+        exact = Fraction(cf) * T / N
+        assert C >= exact or math.isclose(C, float(exact), rel_tol=0, abs_tol=1e-9)
+        assert C - 1 < exact + Fraction(1, 10**9)
+        # cf >= N makes room for the whole batch in any one expert
+        if cf >= N:
+            assert C >= T
+    for bad in [(0, 4, 1.0), (4, 0, 1.0), (4, 4, 0.0), (4, 4, -1.0), (4, 4, float("inf")),
+                (4, 4, float("nan"))]:
+        with pytest.raises(ValueError):
+            O.capacity(*bad)
+
+
+# ---------------------------------------------------------------- aux loss
+def _golden_aux():
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "aux_loss.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if not line:
+                continue
+            tok = line.split()
+            if tok[0] == "case":
+                cur = {"name": tok[1], "N": int(tok[3]), "expected": float(tok[5]), "p": []}
+                cases.append(cur)
+            elif tok[0] == "p":
+                cur["p"].append([float(v) for v in tok[1:]])
+    return cases
+
+
+@pytest.mark.parametrize("case", _golden_aux(), ids=lambda c: c["name"])
+def test_aux_loss_golden(case):
+    p = np.array(case["p"], dtype=np.float64)
+    assert p.shape[1] == case["N"]
+    # routed expert = argmax of the probability row, lowest index on ties
+    e, _ = O.top1(p, p)
+    _, _, counts = O.assign_slots(e, p[np.arange(len(p)), e], case["N"], len(p))
+    assert O.aux_loss(p, counts) == pytest.approx(case["expected"], rel=1e-14, abs=1e-14)
+
+
+def test_aux_loss_zero_router_is_one():
+    # W_g = 0: every logit equal, P_i = 1/N exactly, all tokens tie to expert 0
+    for N in (1, 2, 7, 128):
+        x = np.random.default_rng(N).standard_normal((37, 16))
+        r = O.route(x, np.zeros((N, 16)))
+        assert np.all(r["expert_id"] == 0)
+        np.testing.assert_allclose(r["probs"], 1.0 / N, rtol=0, atol=1e-15)
+        _, _, counts = O.assign_slots(r["expert_id"], r["gate"], N, 37)
+        assert O.aux_loss(r["probs"], counts) == pytest.approx(1.0, abs=1e-14)
+
+
+def test_aux_loss_balanced_routing_is_one():
+    # token t -> expert t mod N (T a multiple of N) gives f_i = 1/N, so
+    # L_aux = sum_i P_i = 1 whatever the probabilities are.
+    rng = np.random.default_rng(1)
+    N, T = 5, 40
+    logits = rng.standard_normal((T, N))
+    for t in range(T):
+        logits[t, t % N] = logits[t].max() + 1.0
+    r = O.route_from_logits(logits)
+    assert np.array_equal(r["expert_id"], np.arange(T) % N)
+    _, _, counts = O.assign_slots(r["expert_id"], r["gate"], N, T)
+    assert O.aux_loss(r["probs"], counts) == pytest.approx(1.0, abs=1e-14)
+
+
+def test_aux_loss_bounds():
+    rng = np.random.default_rng(2)
+    for _ in range(200):
+        N = int(rng.integers(1, 9))
+        T = int(rng.integers(1, 30))
+        r = O.route_from_logits(rng.standard_normal((T, N)) * 3)
+        _, _, counts = O.assign_slots(r["expert_id"], r["gate"], N, T)
+        L = O.aux_loss(r["probs"], counts)
+        assert 0.0 < L <= N + 1e-12
+
+
+# ---------------------------------------------------------------- router
+def test_router_logits_closed_form():
+    # W_g rows = unit vectors e_{k_i}: logit i is coordinate k_i of x, plus bias
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((11, 9))
+    ks = [4, 0, 8, 2]
+    W = np.zeros((4, 9))
+    for i, k in enumerate(ks):
+        W[i, k] = 1.0
+    b = np.array([0.5, -1.0, 0.0, 2.0])
+    l = O.router_logits(x, W, b)
+    assert l.shape == (11, 4)
+    for i, k in enumerate(ks):
+        np.testing.assert_array_equal(l[:, i], x[:, k] + b[i])
+
+
+def test_router_logits_scaled_rows():
+    # W_g = diag(s) restricted to the first N coordinates: logit i = s_i * x_i
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((6, 5))
+    s = np.array([2.0, -3.0, 0.5])
+    W = np.zeros((3, 5))
+    W[np.arange(3), np.arange(3)] = s
+    np.testing.assert_allclose(O.router_logits(x, W), x[:, :3] * s, rtol=0, atol=0)
+
+
+def test_softmax_against_torch():
+    rng = np.random.default_rng(5)
+    l = rng.standard_normal((50, 13)) * 4
+    ref = torch.softmax(torch.from_numpy(l), dim=1).numpy()
+    p = O.softmax(l)
+    np.testing.assert_allclose(p, ref, rtol=1e-13, atol=1e-16)
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+    # shift invariance and overflow safety
+    np.testing.assert_allclose(O.softmax(l + 700.0), p, rtol=1e-12, atol=1e-16)
+
+
+def test_top1_ties_and_gate_closed_form():
+    l = np.array([[0.0, 0.0, 0.0], [1.0, 3.0, 3.0], [2.0, -1.0, 2.0], [-5.0, -4.0, -4.5]])
+    p = O.softmax(l)
+    e, g = O.top1(l, p)
+    assert list(e) == [0, 1, 0, 1]
+    assert g[0] == pytest.approx(1 / 3, abs=1e-15)
+    # two experts: gate = 1 / (1 + exp(-(a - b))) for the winner a
+    rng = np.random.default_rng(6)
+    ab = rng.standard_normal((100, 2)) * 2
+    e, g = O.top1(ab, O.softmax(ab))
+    margin = np.abs(ab[:, 0] - ab[:, 1])
+    np.testing.assert_allclose(g, 1.0 / (1.0 + np.exp(-margin)), rtol=1e-14)
+    assert np.all(e == np.where(ab[:, 1] > ab[:, 0], 1, 0))
+
+
+def test_top1_fast_path_matches_loop():
+    rng = np.random.default_rng(7)
+    l = rng.integers(-2, 3, size=(300, 6)).astype(np.float64)  # many exact ties
+    p = O.softmax(l)
+    e1, g1 = O.top1(l, p)
+    e2, g2 = OM._top1_fast(l, p)
+    assert np.array_equal(e1, e2) and np.array_equal(g1, g2)
+    big = rng.integers(-2, 3, size=(5000, 4)).astype(np.float64)
+    r = O.route_from_logits(big)
+    for t in range(0, 5000, 97):
+        row = list(big[t])
+        assert r["expert_id"][t] == row.index(max(row))
+
+
+# ---------------------------------------------------------------- slots
+def _brute(expert_id, gate, C, mode):
+    """Definition: a token is kept iff fewer than C tokens of its expert come
+    before it in priority order; its slot is that count."""
+    T = len(expert_id)
+    slot = np.full(T, -1)
+    for t in range(T):
+        ahead = 0
+        for u in range(T):
+            if u == t or expert_id[u] != expert_id[t]:
+                continue
+            if mode == O.TOKEN_ORDER:
+                ahead += u < t
+            else:
+                ahead += (gate[u] > gate[t]) or (gate[u] == gate[t] and u < t)
+        if ahead < C:
+            slot[t] = ahead
+    return slot
+
+
+@pytest.mark.parametrize("mode", [O.TOKEN_ORDER, O.GATE_PRIORITY])
+def test_assign_slots_bruteforce_all_assignments(mode):
+    rng = np.random.default_rng(8)
+    for N in (1, 2, 3):
+        for T in range(1, 7 if N == 3 else 8):
+            for assign in itertools.product(range(N), repeat=T):
+                e = np.array(assign)
+                gate = rng.permutation(T) / T + 0.01         # distinct gates
+                if mode == O.GATE_PRIORITY and T >= 3 and rng.random() < 0.3:
+                    gate[rng.integers(T)] = gate[rng.integers(T)]  # plant a tie
+                for C in range(1, T + 1):
+                    slot, drop, counts = O.assign_slots(e, gate, N, C, mode)
+                    ref = _brute(e, gate, C, mode)
+                    assert np.array_equal(slot, ref), (mode, N, T, assign, C)
+                    assert np.array_equal(drop, (ref < 0).astype(np.uint8))
+                    assert np.array_equal(counts, np.bincount(e, minlength=N))
+
+
+@pytest.mark.parametrize("mode", [O.TOKEN_ORDER, O.GATE_PRIORITY])
+def test_assign_slots_invariants(mode):
+    rng = np.random.default_rng(9)
+    for _ in range(50):
+        N = int(rng.integers(1, 9))
+        T = int(rng.integers(1, 400))
+        C = int(rng.integers(1, T + 1))
+        e = rng.integers(0, N, size=T)
+        g = rng.random(T)
+        slot, drop, counts = O.assign_slots(e, g, N, C, mode)
+        assert counts.sum() == T
+        for i in range(N):
+            mine = np.nonzero(e == i)[0]
+            kept = mine[slot[mine] >= 0]
+            assert kept.size == min(counts[i], C)
+            assert sorted(slot[kept]) == list(range(kept.size))     # a permutation
+            dropped = mine[slot[mine] < 0]
+            if mode == O.TOKEN_ORDER:
+                assert np.all(np.diff(slot[kept]) > 0)              # rises with t
+                if dropped.size:
+                    assert kept.max() < dropped.min()
+            elif dropped.size and kept.size:
+                assert g[kept].min() >= g[dropped].max()
+
+
+def test_zero_router_keeps_first_C_tokens():
+    # W_g = 0, cf = 1: every token goes to expert 0 and exactly 0..C-1 are kept
+    T, N, d = 40, 4, 8
+    x = np.random.default_rng(10).standard_normal((T, d))
+    r = O.route(x, np.zeros((N, d)))
+    C = O.capacity(T, N, 1.0)
+    for mode in (O.TOKEN_ORDER, O.GATE_PRIORITY):
+        slot, drop, counts = O.assign_slots(r["expert_id"], r["gate"], N, C, mode)
+        assert np.array_equal(slot[:C], np.arange(C))
+        assert np.all(slot[C:] == -1)
+        assert list(counts) == [T, 0, 0, 0]
+
+
+def test_no_drops_when_cf_at_least_N():
+    rng = np.random.default_rng(11)
+    for _ in range(20):
+        N = int(rng.integers(1, 9))
+        T = int(rng.integers(1, 300))
+        C = O.capacity(T, N, float(N) + rng.random())
+        e = rng.integers(0, N, size=T)
+        for mode in (O.TOKEN_ORDER, O.GATE_PRIORITY):
+            _, drop, _ = O.assign_slots(e, rng.random(T), N, C, mode)
+            assert drop.sum() == 0
+
+
+def test_batch_composition_dependence():
+    # With C fixed, appending tokens never changes earlier tokens in token
+    # order; in gate priority a later, higher-gate token can evict one.
+    rng = np.random.default_rng(12)
+    for _ in range(30):
+        N, T0, T1, C = 3, 30, 50, 6
+        e = rng.integers(0, N, size=T0 + T1)
+        g = rng.random(T0 + T1)
+        s0, _, _ = O.assign_slots(e[:T0], g[:T0], N, C, O.TOKEN_ORDER)
+        s1, _, _ = O.assign_slots(e, g, N, C, O.TOKEN_ORDER)
+        assert np.array_equal(s0, s1[:T0])
+    e = np.array([0, 0, 0])
+    g = np.array([0.5, 0.4, 0.9])
+    s0, _, _ = O.assign_slots(e[:2], g[:2], 1, 2, O.GATE_PRIORITY)
+    s1, _, _ = O.assign_slots(e, g, 1, 2, O.GATE_PRIORITY)
+    assert list(s0) == [0, 1] and list(s1) == [1, -1, 0]
+    # through the real capacity, C grows with T: token order only gains keeps
+    for _ in range(30):
+        e = rng.integers(0, 4, size=80)
+        g = rng.random(80)
+        a, _, _ = O.assign_slots(e[:40], g[:40], 4, O.capacity(40, 4, 1.0))
+        b, _, _ = O.assign_slots(e, g, 4, O.capacity(80, 4, 1.0))
+        assert np.all((a[:40] < 0) | (b[:40] >= 0))
+
+
+# ---------------------------------------------------------------- expert FFN
+def test_expert_ffn_permutation_closed_form():
+    # W1 = permutation P, W2 = signed permutation Q: o = Q relu(P x), by indexing
+    rng = np.random.default_rng(13)
+    n = 7
+    pi = rng.permutation(n)
+    sigma = rng.permutation(n)
+    sgn = rng.choice([-1.0, 2.0], size=n)
+    W1 = np.zeros((n, n))
+    W1[np.arange(n), pi] = 1.0            # (W1 x)_f = x[pi[f]]
+    W2 = np.zeros((n, n))
+    W2[np.arange(n), sigma] = sgn         # (W2 h)_j = sgn_j * h[sigma[j]]
+    x = rng.standard_normal((9, n))
+    o = O.expert_ffn(x, W1, W2)
+    h = np.maximum(x[:, pi], 0.0)
+    np.testing.assert_array_equal(o, sgn[None, :] * h[:, sigma])
+
+
+def test_expert_ffn_rectangular_against_torch():
+    rng = np.random.default_rng(14)
+    d, F = 12, 40
+    x = rng.standard_normal((17, d))
+    W1 = rng.standard_normal((F, d))
+    W2 = rng.standard_normal((d, F))
+    tx, t1, t2 = (torch.from_numpy(a) for a in (x, W1, W2))
+    ref = torch.nn.functional.linear(torch.relu(torch.nn.functional.linear(tx, t1)), t2).numpy()
+    np.testing.assert_allclose(O.expert_ffn(x, W1, W2), ref, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- whole layer
+@pytest.mark.parametrize("gm", [0, 1])
+def test_single_expert_is_dense_ffn(gm):
+    # N = 1, cf >= 1: C >= T, gate = softmax of one logit = 1 exactly
+    rng = np.random.default_rng(15)
+    T, d, F = 33, 10, 24
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((1, d))
+    W1 = rng.standard_normal((1, F, d))
+    W2 = rng.standard_normal((1, d, F))
+    out = O.forward(x, Wg, W1, W2, 1.0, gate_multiply=gm)
+    assert np.all(out["gate"] == 1.0) and out["drop"].sum() == 0
+    tx = torch.from_numpy(x)
+    ref = torch.nn.functional.linear(
+        torch.relu(torch.nn.functional.linear(tx, torch.from_numpy(W1[0]))),
+        torch.from_numpy(W2[0])).numpy()
+    np.testing.assert_allclose(out["y"], ref, rtol=1e-12, atol=1e-12)
+    assert out["aux_loss"] == pytest.approx(1.0, abs=1e-15)
+
+
+def test_gate_flag_drop_and_shared():
+    rng = np.random.default_rng(16)
+    T, d, F, N = 50, 6, 10, 3
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((N, d))
+    W1 = rng.standard_normal((N, F, d))
+    W2 = rng.standard_normal((N, d, F))
+    W1s = rng.standard_normal((F, d))
+    W2s = rng.standard_normal((d, F))
+    a = O.forward(x, Wg, W1, W2, 0.5, gate_multiply=1)
+    b = O.forward(x, Wg, W1, W2, 0.5, gate_multiply=0)
+    c = O.forward(x, Wg, W1, W2, 0.5, gate_multiply=1, W1s=W1s, W2s=W2s)
+    assert a["drop"].sum() > 0
+    for t in range(T):
+        if a["drop"][t]:
+            assert np.all(a["y"][t] == 0.0) and np.all(b["y"][t] == 0.0)
+        else:
+            e = a["expert_id"][t]
+            o = W2[e] @ np.maximum(W1[e] @ x[t], 0)
+            np.testing.assert_allclose(b["y"][t], o, rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(a["y"][t], a["gate"][t] * o, rtol=1e-12, atol=1e-12)
+        S = W2s @ np.maximum(W1s @ x[t], 0)
+        np.testing.assert_allclose(c["y"][t] - a["y"][t], S, rtol=1e-10, atol=1e-10)
+
+
+def test_expert_relabelling_equivariance():
+    rng = np.random.default_rng(17)
+    T, d, F, N = 64, 8, 12, 5
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((N, d))
+    W1 = rng.standard_normal((N, F, d))
+    W2 = rng.standard_normal((N, d, F))
+    perm = rng.permutation(N)
+    a = O.forward(x, Wg, W1, W2, 1.0)
+    b = O.forward(x, Wg[perm], W1[perm], W2[perm], 1.0)
+    inv = np.argsort(perm)
+    assert np.array_equal(inv[a["expert_id"]], b["expert_id"])
+    assert np.array_equal(a["counts"][perm], b["counts"])
+    assert np.array_equal(a["slot"], b["slot"])
+    np.testing.assert_allclose(a["y"], b["y"], rtol=1e-13, atol=1e-13)
+    assert a["aux_loss"] == pytest.approx(b["aux_loss"], rel=1e-13)
+
+
+def test_forward_rows_matches_forward():
+    rng = np.random.default_rng(18)
+    T, d, F, N = 90, 8, 16, 4
+    x = rng.standard_normal((T, d))
+    Wg = rng.standard_normal((N, d))
+    W1 = rng.standard_normal((N, F, d))
+    W2 = rng.standard_normal((N, d, F))
+    W1s = rng.standard_normal((F, d))
+    W2s = rng.standard_normal((d, F))
+    full = O.forward(x, Wg, W1, W2, 0.75, O.GATE_PRIORITY, W1s=W1s, W2s=W2s)
+    rows = rng.choice(T, 25, replace=False)
+    part = O.forward_rows(rows, x, full["expert_id"], full["gate"], full["slot"], 1,
+                          lambda e: (W1[e], W2[e]), W1s, W2s)
+    np.testing.assert_allclose(part, full["y"][rows], rtol=1e-13, atol=1e-13)
