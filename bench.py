@@ -1,0 +1,380 @@
+#!/usr/bin/env python3
+"""Benchmark of the Switch top-1 MoE layer forward on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config base]
+    python bench.py --impl reference ...      # the CPU oracle, timed alone
+
+One step = one switch_moe_forward() over one batch of the workload
+(router, scan + L_aux, slot assignment + dispatch, expert GEMM 1, expert
+GEMM 2, combine).  Prints ONE JSON line (rank 0):
+
+  value      tokens/s of the whole job, inputs resident in HBM, timed with
+             CUDA events over exactly K steps between barriers
+  e2e        the same through switch_moe_forward_hostio(): x copied from
+             pinned host memory and every output copied back inside the
+             timed region
+  roofline   the expert GEMMs (the dominant kernel) against the measured
+             HBM copy bandwidth, from per-phase CUDA events on the stream
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
+
+With --gpus N > 1 (launched by torch.distributed.run) every rank runs an
+independent replica of the layer on its own GPU: the forward has no data
+exchange, so there is no collective on the data path; only the barriers and
+the max-over-ranks of the timed region use the process group.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import CONFIGS, expert_weights, make_inputs, zipf_bias  # noqa: E402
+
+FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+CPU_SAMPLE_EXPERTS = 16
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ oracle sample
+def oracle_sample_step(w, seed=0):
+    """One bounded CPU-oracle step on the workload: route the whole batch,
+    then the expert FFN and combine of the tokens routed to the first
+    CPU_SAMPLE_EXPERTS experts.  Returns (tokens processed, seconds)."""
+    import oracle
+    inp = make_inputs(w, seed, device="cpu", with_experts=False)
+    experts = {e: expert_weights(w, e, seed, "cpu") for e in range(min(CPU_SAMPLE_EXPERTS, w.N))}
+    t0 = time.perf_counter()
+    r = oracle.route(inp.x, inp.W_g, zipf_bias(w))
+    C = oracle.capacity(w.T, w.N, w.capacity_factor)
+    slot, drop, counts = oracle.assign_slots(r["expert_id"], r["gate"], w.N, C, w.priority_mode)
+    rows = np.nonzero(r["expert_id"] < len(experts))[0]
+    oracle.forward_rows(rows, inp.x, r["expert_id"], r["gate"], slot, w.gate_multiply,
+                        lambda e: experts[e], inp.W1s, inp.W2s)
+    oracle.aux_loss(r["probs"], counts)
+    return int(rows.size), time.perf_counter() - t0
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def cpu_sample_desc(w):
+    return (f"{w.name} layer: routing of all {w.T} tokens + expert FFN and combine of the "
+            f"tokens routed to experts 0..{min(CPU_SAMPLE_EXPERTS, w.N) - 1} "
+            f"(of {w.N}); value = those tokens / wall time")
+
+
+def run_reference(args, rank, world):
+    w = CONFIGS[args.config]
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample_step(w)
+    tok, sec = 0, 0.0
+    for _ in range(args.steps):
+        n, s = oracle_sample_step(w)
+        tok += n
+        sec += s
+    value = tok / sec
+    cores = blas_threads()
+    line = {
+        "impl": "reference", "metric": "top-1 MoE layer tokens/sec", "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": cpu_sample_desc(w)},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w):
+    return {"workload": f"{w.name}: Switch top-1 MoE layer T={w.T} d_model={w.d_model} "
+                        f"d_ff={w.d_ff} N={w.N} cf={w.capacity_factor} {w.dtype}"
+                        f"{' +shared expert' if w.has_shared else ''}",
+            "T": w.T, "d_model": w.d_model, "d_ff": w.d_ff, "N": w.N,
+            "capacity_factor": w.capacity_factor,
+            "priority": "gate" if w.priority_mode else "token-order",
+            "gate_multiply": w.gate_multiply, "parallelism": "replicas",
+            "l2": "inputs larger than L2: every step streams the active experts' weights "
+                  "(far above the 126 MB L2) from HBM"}
+
+
+# ------------------------------------------------------------------ GPU arm
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--config", default="base", choices=sorted(CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import switch_top_expert_router_b300 as sm
+    sm.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    w = CONFIGS[args.config]
+    inp = make_inputs(w, seed=0, device=dev)
+    p = sm.make_params(w.T, w.d_model, w.d_ff, w.N, w.capacity_factor, w.priority_mode,
+                       w.gate_multiply, sm.BF16 if w.dtype == "bf16" else sm.F32, w.has_shared)
+    ws = sm.workspace(sm.switch_moe_workspace_bytes(p), dev)
+    out = None
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        nonlocal out
+        out = sm.switch_moe_forward(inp.x, inp.W_g, inp.W1, inp.W2, w.capacity_factor,
+                                    w.priority_mode, w.gate_multiply, b_g=inp.b_g,
+                                    W1s=inp.W1s, W2s=inp.W2s, ws=ws, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    rc = sm.switch_moe_sync_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after warm-up: {sm.strerror(rc)}")
+
+    # ---- timed region: exactly K steps
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    rc = sm.switch_moe_sync_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after timing: {sm.strerror(rc)}")
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    value = w.T * args.steps * world / (ms / 1e3)
+
+    # ---- per-phase times (same K steps, events at the phase boundaries)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(sm.NUM_PHASE_EVENTS)]
+          for _ in range(args.steps)]
+    for row in ev:
+        for e in row:
+            e.record(stream)       # materialise the CUDA event handles
+    torch.cuda.synchronize()
+    for row in ev:
+        sm.switch_moe_set_phase_events(row)
+        step()
+    sm.switch_moe_set_phase_events(None)
+    torch.cuda.synchronize()
+    phase_ms = {name: statistics.mean(row[i].elapsed_time(row[i + 1]) for row in ev)
+                for i, name in enumerate(sm.PHASES)}
+
+    # ---- workload facts for the roofline
+    counts = out.expert_counts.cpu().numpy().astype(np.int64)
+    C = sm.switch_moe_capacity(w.T, w.N, w.capacity_factor)
+    kept = np.minimum(counts, C)
+    active = int((kept > 0).sum())
+    T_kept = int(kept.sum())
+    eb = 2 if w.dtype == "bf16" else 4
+    d, F = w.d_model, w.d_ff
+    wbytes_expert = d * F * eb
+    g1_bytes = active * wbytes_expert + T_kept * d * eb + T_kept * F * eb
+    g2_bytes = active * wbytes_expert + T_kept * F * eb + T_kept * d * 4
+    gemm_ms = phase_ms["expert_gemm1"] + phase_ms["expert_gemm2"]
+    hbm, bf16_peak, peak_kind = peaks()
+    achieved = (g1_bytes + g2_bytes) / (gemm_ms / 1e3) / 1e9
+    layer_bytes = (w.T * d * eb + w.T * d * 4 + w.N * d * 4 + w.T * 13 + w.N * 4
+                   + 2 * active * wbytes_expert + (2 * wbytes_expert if w.has_shared else 0))
+    layer_flops = 4.0 * T_kept * d * F + (4.0 * w.T * d * F if w.has_shared else 0.0)
+    t_roof = max(layer_flops / (bf16_peak * 1e12), layer_bytes / (hbm * 1e9))
+    launches = 6 + (2 if w.priority_mode else 0) + (2 if w.has_shared else 0)
+
+    # ---- end to end through the host-buffer entry point
+    e2e = None
+    if not args.no_e2e:
+        x_host = inp.x.cpu().pin_memory()
+        hout = None
+        hws = sm.workspace(sm.switch_moe_hostio_workspace_bytes(p), dev)
+
+        def hstep():
+            nonlocal hout
+            hout = sm.switch_moe_forward_hostio(x_host, inp.W_g, inp.W1, inp.W2,
+                                                w.capacity_factor, w.priority_mode,
+                                                w.gate_multiply, b_g=inp.b_g, W1s=inp.W1s,
+                                                W2s=inp.W2s, ws=hws, out=hout)
+        for _ in range(args.warmup):
+            hstep()
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        h0 = torch.cuda.Event(enable_timing=True)
+        h1 = torch.cuda.Event(enable_timing=True)
+        h0.record(stream)
+        for _ in range(args.steps):
+            hstep()
+        h1.record(stream)
+        torch.cuda.synchronize()
+        hms = h0.elapsed_time(h1)
+        if pg:
+            t = torch.tensor([hms], device=dev)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            hms = float(t.item())
+        e2e = {"value": w.T * args.steps * world / (hms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": w.T * d * eb,
+               "d2h_bytes_per_step": w.T * d * 4 + w.T * 13 + w.N * 4 + 4,
+               "ms_per_step": hms / args.steps}
+        if sm.switch_moe_sync_status() != 0:
+            raise RuntimeError("device status after the host-IO run")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tok, sec = 0, 0.0
+        while sec < 10.0:
+            n, s = oracle_sample_step(w)
+            tok += n
+            sec += s
+        cpu = {"value": tok / sec, "unit": "tokens/s", "cores": blas_threads(),
+               "kind": "oracle", "sample": cpu_sample_desc(w)}
+
+    if rank == 0:
+        line = {
+            "metric": "top-1 MoE layer tokens/sec", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": workload_config(w),
+            "e2e": e2e,
+            "roofline": {"kernel": "gemm_tc_kernel (expert GEMM 1 + 2)", "bound": "hbm",
+                         "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": None,
+                         "algorithmic_bytes_per_launch": (g1_bytes + g2_bytes) / 2},
+            "layer_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": 1e3 * ms / args.steps,
+                               "frac": t_roof / (ms / args.steps / 1e3),
+                               "bytes": layer_bytes, "flops": layer_flops,
+                               "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16_peak,
+                                         "kind": peak_kind}},
+            "phase_us": {k: 1e3 * v for k, v in phase_ms.items()},
+            "routing": {"active_experts": active, "kept_tokens": T_kept,
+                        "dropped": int(w.T - T_kept), "capacity": C,
+                        "aux_loss": float(out.aux_loss.item())},
+            "cpu_baseline": cpu,
+            "gpu_launches": launches * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,586 @@
+// C ABI of libswitchmoe.so: argument checks, workspace plan, TMA tensor
+// maps and the launch sequence of the layer forward.  Declarations and the
+// contract of each entry point are in include/switch_moe.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace smoe {
+
+__device__ int g_status;   // per-device status word, read by switch_moe_sync_status
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+// SM count the K-split heuristic plans for (B300).  The workspace size must
+// not depend on which device is current, so the plan does not query it.
+constexpr int kPlanSMs = 148;
+
+struct DeviceInfo {
+  bool probed = false;
+  bool ok = false;
+  int sms = 0;
+  int* status = nullptr;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+// Current device, checked once: compute capability 10.3 (B300, sm_103a).
+const DeviceInfo* current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.probed) {
+    d.probed = true;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    void* p = nullptr;
+    d.ok = (major == 10 && minor == 3) &&
+           cudaGetSymbolAddress(&p, g_status) == cudaSuccess && d.sms > 0;
+    d.status = static_cast<int*>(p);
+    cudaGetLastError();
+  }
+  return d.ok ? &d : nullptr;
+}
+
+// ----------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+// bf16 matrix [rows, cols] row-major, boxes of 64 columns (128 B) x box_rows,
+// 128-byte swizzle: the K-major operand layout of the tensor-core GEMM.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kTileK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ----------------------------------------------------------- plan
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Plan {
+  int64_t T, d, F, N;
+  int C, R;
+  bool bf16;
+  int mode, gm, shared;
+  int elem;          // bytes per x/W element
+  int BN, BNs;       // token tiles: routed experts, shared expert
+  int max_entries;   // N * ceil(C / BN)
+  int ksplit;        // K splits of the second routed GEMM
+  // workspace offsets
+  size_t o_Ppart, o_hist, o_rank, o_Psum, o_start, o_list, o_entries, o_ctrl, o_xbuf, o_H0, o_H1,
+      o_O, o_Hs0, o_Hs1, o_Os, total;
+  // extra for the host-IO entry point
+  size_t o_xin, o_y, o_eid, o_gate, o_slot, o_drop, o_cnt, o_aux, total_hostio;
+};
+
+int64_t capacity_of(int64_t T, int64_t N, double cf) {
+  if (T < 1 || N < 1 || !(cf > 0.0) || !std::isfinite(cf)) return SWITCH_MOE_ERR_INVALID_ARG;
+  const double c = std::ceil(cf * (double)T / (double)N);
+  if (!(c >= 1.0) || c > 2147483647.0) return SWITCH_MOE_ERR_INVALID_ARG;
+  return (int64_t)c;
+}
+
+int choose_ksplit(int64_t tiles, int k_blocks, int sms) {
+  // Split the long K of the second GEMM only when there are too few tiles
+  // to give every SM at least two.
+  int s = 1;
+  while (s < 8 && tiles * s < 2 * (int64_t)sms && k_blocks % (2 * s) == 0) s *= 2;
+  return s;
+}
+
+int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
+  if (!p) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (p->T < 0 || p->N < 1 || p->d_model < 1 || p->d_ff < 1) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (!(p->capacity_factor > 0.0) || !std::isfinite(p->capacity_factor))
+    return SWITCH_MOE_ERR_INVALID_ARG;
+  if (p->priority_mode != SWITCH_MOE_TOKEN_ORDER && p->priority_mode != SWITCH_MOE_GATE_PRIORITY)
+    return SWITCH_MOE_ERR_INVALID_ARG;
+  if ((p->gate_multiply != 0 && p->gate_multiply != 1) ||
+      (p->has_shared != 0 && p->has_shared != 1) ||
+      (p->dtype != SWITCH_MOE_F32 && p->dtype != SWITCH_MOE_BF16))
+    return SWITCH_MOE_ERR_INVALID_ARG;
+  if (p->N > kMaxExperts) return SWITCH_MOE_ERR_UNSUPPORTED;
+  if (need_gemm && (p->d_model < 8 || p->d_ff < 8 || p->d_model % 8 || p->d_ff % 8))
+    return SWITCH_MOE_ERR_UNSUPPORTED;
+  if (p->T > (int64_t)1 << 30 || p->d_model > (1 << 20) || p->d_ff > (1 << 20))
+    return SWITCH_MOE_ERR_UNSUPPORTED;
+  Plan& q = *pl;
+  std::memset(&q, 0, sizeof(q));
+  q.T = p->T; q.d = p->d_model; q.F = p->d_ff; q.N = p->N;
+  q.bf16 = p->dtype == SWITCH_MOE_BF16;
+  q.elem = q.bf16 ? 2 : 4;
+  q.mode = p->priority_mode; q.gm = p->gate_multiply; q.shared = p->has_shared;
+  if (q.T == 0) return SWITCH_MOE_OK;
+  const int64_t C = capacity_of(q.T, q.N, p->capacity_factor);
+  if (C < 1) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (q.N * C > ((int64_t)1 << 30)) return SWITCH_MOE_ERR_UNSUPPORTED;
+  if (q.mode == SWITCH_MOE_GATE_PRIORITY && (C < q.T ? C : q.T) > kGateSortMax)
+    return SWITCH_MOE_ERR_UNSUPPORTED;
+  q.C = (int)C;
+  q.R = (int)cdiv(q.T, kRouterTM);
+  if (q.bf16) {
+    q.BN = (int)(cdiv(C, 16) * 16 < 256 ? cdiv(C, 16) * 16 : 256);
+    q.BNs = (int)(cdiv(q.T, 16) * 16 < 256 ? cdiv(q.T, 16) * 16 : 256);
+  } else {
+    q.BN = kSimtTileN;
+    q.BNs = kSimtTileN;
+  }
+  q.max_entries = (int)(q.N * cdiv(C, q.BN));
+  q.ksplit = 1;
+  if (q.bf16 && need_gemm) {
+    const int k2 = (int)cdiv(q.F, kTileK);
+    q.ksplit = choose_ksplit((int64_t)q.max_entries * cdiv(q.d, kTileM), k2, kPlanSMs);
+  }
+  const int64_t NC = q.N * C;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+  q.o_Ppart = take((size_t)q.R * q.N * 4);
+  q.o_hist = take((size_t)q.R * q.N * 4);
+  q.o_rank = take((size_t)q.T * 4);
+  q.o_Psum = take((size_t)q.N * 4);
+  q.o_start = take((size_t)(q.N + 1) * 4);
+  q.o_list = take((size_t)q.T * 4);
+  q.o_entries = take((size_t)q.max_entries * 8);
+  q.o_ctrl = take(64);
+  if (need_gemm) {
+    q.o_xbuf = take((size_t)NC * q.d * q.elem);
+    if (q.bf16) {
+      q.o_H0 = take((size_t)NC * q.F * 2);
+      q.o_H1 = take((size_t)NC * q.F * 2);
+    } else {
+      q.o_H0 = take((size_t)NC * q.F * 4);
+    }
+    q.o_O = take((size_t)q.ksplit * NC * q.d * 4);
+    if (q.shared) {
+      if (q.bf16) {
+        q.o_Hs0 = take((size_t)q.T * q.F * 2);
+        q.o_Hs1 = take((size_t)q.T * q.F * 2);
+      } else {
+        q.o_Hs0 = take((size_t)q.T * q.F * 4);
+      }
+      q.o_Os = take((size_t)q.T * q.d * 4);
+    }
+  }
+  q.total = o;
+  q.o_xin = take((size_t)q.T * q.d * q.elem);
+  q.o_y = take((size_t)q.T * q.d * 4);
+  q.o_eid = take((size_t)q.T * 4);
+  q.o_gate = take((size_t)q.T * 4);
+  q.o_slot = take((size_t)q.T * 4);
+  q.o_drop = take((size_t)q.T);
+  q.o_cnt = take((size_t)q.N * 4);
+  q.o_aux = take(4);
+  q.total_hostio = o;
+  return SWITCH_MOE_OK;
+}
+
+inline bool al(const void* ptr, size_t a) { return ((uintptr_t)ptr % a) == 0; }
+
+// Phase events of switch_moe_set_phase_events (per host thread).
+thread_local cudaEvent_t t_phase[SWITCH_MOE_NUM_PHASE_EVENTS];
+thread_local bool t_phase_on = false;
+inline void mark(int i, cudaStream_t s) {
+  if (t_phase_on) cudaEventRecord(t_phase[i], s);
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+// Routing: router -> scan -> slot assignment (-> gate ranking -> dispatch).
+// x == nullptr routes `logits` instead of computing them.
+int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g,
+                const float* logits, int32_t* expert_id, float* gate, int32_t* slot,
+                uint8_t* drop, int32_t* counts, float* aux, void* ws, bool dispatch,
+                int* status, cudaStream_t s) {
+  int32_t* ctrl = at<int32_t>(ws, q.o_ctrl);
+  RouterArgs ra{};
+  ra.x = x; ra.W_g = W_g; ra.b_g = b_g; ra.logits_in = logits; ra.logits_out = nullptr;
+  ra.T = (int)q.T; ra.d = (int)q.d; ra.N = (int)q.N; ra.x_is_bf16 = q.bf16;
+  ra.expert_id = expert_id; ra.gate = gate;
+  ra.P_part = at<float>(ws, q.o_Ppart); ra.hist = at<int32_t>(ws, q.o_hist);
+  ra.local_rank = at<int32_t>(ws, q.o_rank); ra.ctrl = ctrl;
+  mark(0, s);
+  if (launch_router(ra, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  mark(1, s);
+
+  ScanArgs sa{};
+  sa.hist = ra.hist; sa.P_part = ra.P_part; sa.R = q.R; sa.N = (int)q.N; sa.T = (int)q.T;
+  sa.C = q.C; sa.counts = counts; sa.P_sum = at<float>(ws, q.o_Psum);
+  sa.expert_start = at<int32_t>(ws, q.o_start); sa.aux_loss = aux;
+  sa.entries = at<int2>(ws, q.o_entries); sa.BN = q.BN; sa.ctrl = ctrl;
+  if (launch_scan(sa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  mark(2, s);
+
+  AssignArgs aa{};
+  aa.T = (int)q.T; aa.N = (int)q.N; aa.C = q.C; aa.d = (int)q.d; aa.elem_bytes = q.elem;
+  aa.mode = q.mode; aa.expert_id = expert_id; aa.gate = gate; aa.bases = ra.hist;
+  aa.local_rank = ra.local_rank; aa.counts = counts; aa.expert_start = sa.expert_start;
+  aa.sorted_list = at<int32_t>(ws, q.o_list); aa.slot = slot; aa.drop = drop;
+  aa.x = dispatch ? x : nullptr; aa.xbuf = dispatch ? at<void>(ws, q.o_xbuf) : nullptr;
+  aa.status = status;
+  if (launch_assign(aa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  if (q.mode == SWITCH_MOE_GATE_PRIORITY) {
+    if (launch_gate_select(aa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+    if (dispatch && launch_dispatch(aa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  }
+  mark(3, s);
+  return SWITCH_MOE_OK;
+}
+
+// One tensor-core or SIMT GEMM over routed work items or a dense problem.
+int run_gemm(const Plan& q, const DeviceInfo* dev, bool dense, int layer, const void* A,
+             const void* B0, const void* B1, void* out0, void* out1, const int32_t* counts,
+             void* ws, cudaStream_t s) {
+  GemmArgs g{};
+  const int64_t M = layer == 1 ? q.F : q.d;
+  const int64_t K = layer == 1 ? q.d : q.F;
+  const int64_t rows = dense ? q.T : q.C;
+  g.M = (int)M; g.K = (int)K; g.rows_per_expert = (int)rows;
+  g.BN = dense ? q.BNs : q.BN;
+  g.entries = dense ? nullptr : at<int2>(ws, q.o_entries);
+  g.n_entries = dense ? nullptr : at<int32_t>(ws, q.o_ctrl) + 1;
+  g.n_entries_dense = dense ? (int)cdiv(q.T, g.BN) : 0;
+  g.counts = dense ? nullptr : counts;
+  g.cap = q.C;
+  g.epi = layer == 1 ? 0 : 1;
+  g.out0 = out0; g.out1 = out1;
+  g.ldo = (int)M;
+  g.status = dev->status;
+  const int64_t n_ent_max = dense ? g.n_entries_dense : q.max_entries;
+  if (q.bf16) {
+    g.m_tiles = (int)cdiv(M, kTileM);
+    g.ksplit = (layer == 2 && !dense) ? q.ksplit : 1;
+    g.k_blocks = (int)(cdiv(K, kTileK) / g.ksplit);
+    g.num_b = layer == 1 ? 1 : 2;
+    g.split_stride = (size_t)q.N * q.C * q.d;
+    g.stages = gemm_tc_max_stages(g.BN, g.num_b);
+    g.smem_bytes = gemm_tc_smem_bytes(g.BN, g.num_b, g.stages);
+    const int64_t tiles_max = n_ent_max * g.m_tiles * g.ksplit;
+    g.grid = (int)(tiles_max < dev->sms ? tiles_max : dev->sms);
+    if (g.grid < 1) return SWITCH_MOE_OK;
+    const int64_t brows = dense ? q.T : q.N * q.C;
+    CUtensorMap ta, tb0, tb1;
+    if (!make_map(&ta, A, (uint64_t)((dense ? 1 : q.N) * M), (uint64_t)K, kTileM) ||
+        !make_map(&tb0, B0, (uint64_t)brows, (uint64_t)K, (uint32_t)g.BN))
+      return SWITCH_MOE_ERR_CUDA;
+    if (g.num_b == 2) {
+      if (!make_map(&tb1, B1, (uint64_t)brows, (uint64_t)K, (uint32_t)g.BN))
+        return SWITCH_MOE_ERR_CUDA;
+    } else {
+      tb1 = tb0;
+    }
+    if (launch_gemm_tc(g, ta, tb0, tb1, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  } else {
+    g.m_tiles = (int)cdiv(M, 64);
+    g.ksplit = 1;
+    g.k_blocks = 0;
+    g.num_b = 1;
+    g.split_stride = (size_t)q.N * q.C * q.d;
+    const int64_t tiles_max = n_ent_max * g.m_tiles;
+    g.grid = (int)tiles_max;
+    if (launch_gemm_simt(g, static_cast<const float*>(A), static_cast<const float*>(B0), s) !=
+        cudaSuccess)
+      return SWITCH_MOE_ERR_CUDA;
+  }
+  return SWITCH_MOE_OK;
+}
+
+int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const float* W_g,
+                   const float* b_g, const void* W1, const void* W2, const void* W1s,
+                   const void* W2s, float* y, int32_t* expert_id, float* gate, int32_t* slot,
+                   uint8_t* drop, int32_t* counts, float* aux, void* ws, cudaStream_t s) {
+  int rc = run_routing(q, x, W_g, b_g, nullptr, expert_id, gate, slot, drop, counts, aux, ws,
+                       true, dev->status, s);
+  if (rc) return rc;
+  void* xbuf = at<void>(ws, q.o_xbuf);
+  void* H0 = at<void>(ws, q.o_H0);
+  void* H1 = q.bf16 ? at<void>(ws, q.o_H1) : nullptr;
+  float* O = at<float>(ws, q.o_O);
+  if ((rc = run_gemm(q, dev, false, 1, W1, xbuf, nullptr, H0, H1, counts, ws, s))) return rc;
+  mark(4, s);
+  float* Os = nullptr;
+  if (q.shared) {
+    void* Hs0 = at<void>(ws, q.o_Hs0);
+    void* Hs1 = q.bf16 ? at<void>(ws, q.o_Hs1) : nullptr;
+    Os = at<float>(ws, q.o_Os);
+    if ((rc = run_gemm(q, dev, true, 1, W1s, x, nullptr, Hs0, Hs1, nullptr, ws, s))) return rc;
+    if ((rc = run_gemm(q, dev, true, 2, W2s, Hs0, Hs1, Os, nullptr, nullptr, ws, s))) return rc;
+  }
+  mark(5, s);
+  if ((rc = run_gemm(q, dev, false, 2, W2, H0, H1, O, nullptr, counts, ws, s))) return rc;
+  mark(6, s);
+  CombineArgs ca{};
+  ca.T = (int)q.T; ca.d = (int)q.d; ca.C = q.C;
+  ca.ksplit = q.bf16 ? q.ksplit : 1;
+  ca.gate_multiply = q.gm; ca.expert_id = expert_id; ca.gate = gate; ca.slot = slot;
+  ca.O = O; ca.split_stride = (size_t)q.N * q.C * q.d; ca.S = Os; ca.y = y;
+  if (launch_combine(ca, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  mark(7, s);
+  return SWITCH_MOE_OK;
+}
+
+int empty_batch(int32_t* counts, float* aux, int64_t N, cudaStream_t s) {
+  if (cudaMemsetAsync(counts, 0, (size_t)N * 4, s) != cudaSuccess ||
+      cudaMemsetAsync(aux, 0, 4, s) != cudaSuccess)
+    return SWITCH_MOE_ERR_CUDA;
+  return SWITCH_MOE_OK;
+}
+
+}  // namespace
+
+int* device_status_ptr() {
+  const DeviceInfo* d = current_device();
+  return d ? d->status : nullptr;
+}
+
+}  // namespace smoe
+
+using namespace smoe;
+
+extern "C" {
+
+int64_t switch_moe_capacity(int64_t T, int64_t N, double capacity_factor) {
+  return capacity_of(T, N, capacity_factor);
+}
+
+int switch_moe_workspace_bytes(const switch_moe_params* p, size_t* bytes) {
+  if (!bytes) return SWITCH_MOE_ERR_INVALID_ARG;
+  Plan q;
+  const int rc = make_plan(p, &q, true);
+  if (rc) return rc;
+  *bytes = q.total;
+  return SWITCH_MOE_OK;
+}
+
+int switch_moe_hostio_workspace_bytes(const switch_moe_params* p, size_t* bytes) {
+  if (!bytes) return SWITCH_MOE_ERR_INVALID_ARG;
+  Plan q;
+  const int rc = make_plan(p, &q, true);
+  if (rc) return rc;
+  *bytes = q.total_hostio;
+  return SWITCH_MOE_OK;
+}
+
+int switch_moe_forward(const switch_moe_params* p, const void* x, const float* W_g,
+                       const float* b_g, const void* W1, const void* W2, const void* W1s,
+                       const void* W2s, float* y, int32_t* expert_id, float* gate, int32_t* slot,
+                       uint8_t* drop_mask, int32_t* expert_counts, float* aux_loss,
+                       void* workspace, size_t workspace_bytes, switch_moe_stream_t stream) {
+  Plan q;
+  int rc = make_plan(p, &q, true);
+  if (rc) return rc;
+  if (!expert_counts || !aux_loss) return SWITCH_MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = current_device();
+  if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (q.T == 0) return empty_batch(expert_counts, aux_loss, q.N, s);
+  if (!x || !W_g || !W1 || !W2 || !y || !expert_id || !gate || !slot || !drop_mask || !workspace)
+    return SWITCH_MOE_ERR_INVALID_ARG;
+  if (q.shared && (!W1s || !W2s)) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (!al(x, 16) || !al(W_g, 16) || !al(W1, 16) || !al(W2, 16) || !al(y, 16) ||
+      !al(workspace, 256) || !al(expert_id, 4) || !al(gate, 4) || !al(slot, 4) ||
+      !al(expert_counts, 4) || !al(aux_loss, 4) || (b_g && !al(b_g, 4)) ||
+      (q.shared && (!al(W1s, 16) || !al(W2s, 16))))
+    return SWITCH_MOE_ERR_ALIGNMENT;
+  if (workspace_bytes < q.total) return SWITCH_MOE_ERR_WORKSPACE_TOO_SMALL;
+  return forward_device(q, dev, x, W_g, b_g, W1, W2, W1s, W2s, y, expert_id, gate, slot,
+                        drop_mask, expert_counts, aux_loss, workspace, s);
+}
+
+int switch_moe_forward_hostio(const switch_moe_params* p, const void* x_host, const float* W_g,
+                              const float* b_g, const void* W1, const void* W2, const void* W1s,
+                              const void* W2s, float* y_host, int32_t* expert_id_host,
+                              float* gate_host, int32_t* slot_host, uint8_t* drop_mask_host,
+                              int32_t* expert_counts_host, float* aux_loss_host, void* workspace,
+                              size_t workspace_bytes, switch_moe_stream_t stream) {
+  Plan q;
+  int rc = make_plan(p, &q, true);
+  if (rc) return rc;
+  const DeviceInfo* dev = current_device();
+  if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
+  if (!x_host || !W_g || !W1 || !W2 || !y_host || !expert_id_host || !gate_host || !slot_host ||
+      !drop_mask_host || !expert_counts_host || !aux_loss_host || !workspace)
+    return SWITCH_MOE_ERR_INVALID_ARG;
+  if (q.shared && (!W1s || !W2s)) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (!al(W_g, 16) || !al(W1, 16) || !al(W2, 16) || !al(workspace, 256) ||
+      (q.shared && (!al(W1s, 16) || !al(W2s, 16))))
+    return SWITCH_MOE_ERR_ALIGNMENT;
+  if (workspace_bytes < q.total_hostio) return SWITCH_MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int32_t* d_cnt = at<int32_t>(workspace, q.o_cnt);
+  float* d_aux = at<float>(workspace, q.o_aux);
+  if (q.T == 0) {
+    if ((rc = empty_batch(d_cnt, d_aux, q.N, s))) return rc;
+  } else {
+    void* d_x = at<void>(workspace, q.o_xin);
+    if (cudaMemcpyAsync(d_x, x_host, (size_t)q.T * q.d * q.elem, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+      return SWITCH_MOE_ERR_CUDA;
+    // device copies of the outputs live after the forward's own region
+    rc = forward_device(q, dev, d_x, W_g, b_g, W1, W2, W1s, W2s, at<float>(workspace, q.o_y),
+                        at<int32_t>(workspace, q.o_eid), at<float>(workspace, q.o_gate),
+                        at<int32_t>(workspace, q.o_slot), at<uint8_t>(workspace, q.o_drop), d_cnt,
+                        d_aux, workspace, s);
+    if (rc) return rc;
+    const size_t T = (size_t)q.T;
+    if (cudaMemcpyAsync(y_host, at<void>(workspace, q.o_y), T * q.d * 4, cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess ||
+        cudaMemcpyAsync(expert_id_host, at<void>(workspace, q.o_eid), T * 4,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(gate_host, at<void>(workspace, q.o_gate), T * 4, cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess ||
+        cudaMemcpyAsync(slot_host, at<void>(workspace, q.o_slot), T * 4, cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess ||
+        cudaMemcpyAsync(drop_mask_host, at<void>(workspace, q.o_drop), T, cudaMemcpyDeviceToHost,
+                        s) != cudaSuccess)
+      return SWITCH_MOE_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(expert_counts_host, d_cnt, (size_t)q.N * 4, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(aux_loss_host, d_aux, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SWITCH_MOE_ERR_CUDA;
+  return SWITCH_MOE_OK;
+}
+
+int switch_moe_route_from_logits(const switch_moe_params* p, const float* logits,
+                                 int32_t* expert_id, float* gate, int32_t* slot,
+                                 uint8_t* drop_mask, int32_t* expert_counts, float* aux_loss,
+                                 void* workspace, size_t workspace_bytes,
+                                 switch_moe_stream_t stream) {
+  if (!p) return SWITCH_MOE_ERR_INVALID_ARG;
+  switch_moe_params pr = *p;
+  pr.d_model = 8;
+  pr.d_ff = 8;
+  pr.has_shared = 0;
+  Plan q;
+  int rc = make_plan(&pr, &q, false);
+  if (rc) return rc;
+  if (!expert_counts || !aux_loss) return SWITCH_MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = current_device();
+  if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (q.T == 0) return empty_batch(expert_counts, aux_loss, q.N, s);
+  if (!logits || !expert_id || !gate || !slot || !drop_mask || !workspace)
+    return SWITCH_MOE_ERR_INVALID_ARG;
+  if (!al(logits, 4) || !al(workspace, 256) || !al(expert_id, 4) || !al(gate, 4) ||
+      !al(slot, 4) || !al(expert_counts, 4) || !al(aux_loss, 4))
+    return SWITCH_MOE_ERR_ALIGNMENT;
+  if (workspace_bytes < q.total) return SWITCH_MOE_ERR_WORKSPACE_TOO_SMALL;
+  const bool on = t_phase_on;
+  t_phase_on = false;   // phase events belong to the forward calls only
+  rc = run_routing(q, nullptr, nullptr, nullptr, logits, expert_id, gate, slot, drop_mask,
+                   expert_counts, aux_loss, workspace, false, dev->status, s);
+  t_phase_on = on;
+  return rc;
+}
+
+int switch_moe_router_logits(const switch_moe_params* p, const void* x, const float* W_g,
+                             const float* b_g, float* logits, switch_moe_stream_t stream) {
+  Plan q;
+  int rc = make_plan(p, &q, false);
+  if (rc) return rc;
+  const DeviceInfo* dev = current_device();
+  if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
+  if (q.T == 0) return SWITCH_MOE_OK;
+  if (!x || !W_g || !logits) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (q.d % 8) return SWITCH_MOE_ERR_UNSUPPORTED;
+  if (!al(x, 16) || !al(W_g, 16) || !al(logits, 4) || (b_g && !al(b_g, 4)))
+    return SWITCH_MOE_ERR_ALIGNMENT;
+  RouterArgs ra{};
+  ra.x = x; ra.W_g = W_g; ra.b_g = b_g; ra.logits_out = logits;
+  ra.T = (int)q.T; ra.d = (int)q.d; ra.N = (int)q.N; ra.x_is_bf16 = q.bf16;
+  if (launch_router(ra, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SWITCH_MOE_ERR_CUDA;
+  return SWITCH_MOE_OK;
+}
+
+int switch_moe_sync_status(switch_moe_stream_t stream) {
+  const DeviceInfo* dev = current_device();
+  if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SWITCH_MOE_ERR_CUDA;
+  int v = 0;
+  const int zero = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return SWITCH_MOE_ERR_CUDA;
+  return v;
+}
+
+const char* switch_moe_strerror(int code) {
+  switch (code) {
+    case SWITCH_MOE_OK: return "ok";
+    case SWITCH_MOE_ERR_INVALID_ARG: return "invalid argument";
+    case SWITCH_MOE_ERR_ALIGNMENT: return "misaligned pointer";
+    case SWITCH_MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case SWITCH_MOE_ERR_UNSUPPORTED: return "shape outside the supported range";
+    case SWITCH_MOE_ERR_CUDA: return "CUDA runtime or launch error";
+    case SWITCH_MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case SWITCH_MOE_ERR_NO_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status code";
+  }
+}
+
+int switch_moe_set_phase_events(void* const* events, int n) {
+  if (!events) {
+    t_phase_on = false;
+    return SWITCH_MOE_OK;
+  }
+  if (n != SWITCH_MOE_NUM_PHASE_EVENTS) return SWITCH_MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n; ++i) {
+    if (!events[i]) return SWITCH_MOE_ERR_INVALID_ARG;
+    t_phase[i] = static_cast<cudaEvent_t>(events[i]);
+  }
+  t_phase_on = true;
+  return SWITCH_MOE_OK;
+}
+
+int switch_moe_selftest_wait_timeout(uint64_t timeout_ns, switch_moe_stream_t stream) {
+  const DeviceInfo* dev = current_device();
+  if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
+  unsigned long long t = timeout_ns;
+  if (t < 1000000ull) t = 1000000ull;
+  if (t > 2000000000ull) t = 2000000000ull;
+  if (launch_selftest_wait(dev->status, t, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return SWITCH_MOE_ERR_CUDA;
+  return SWITCH_MOE_OK;
+}
+
+int switch_moe_version(void) { return 100; }
+
+}  // extern "C"

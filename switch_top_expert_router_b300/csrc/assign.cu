@@ -1,0 +1,319 @@
+// Capacity-limited slot assignment, overflow, dispatch into the per-expert
+// buffer, and the auxiliary-loss reduction.
+//
+// Sources: "Top-1 路由 (Top-1 Routing)" (compassingai.com), Token Dropping
+// section (an expert takes at most capacity tokens; the rest skip it) and
+// load-balancing section (L_aux = N * sum_i f_i P_i); Switch Transformer
+// walk-through (personwebsite.pages.dev/moe-switch), expert-capacity section;
+// "MoE 专家容量因子与 Token 丢弃" (wiblog.cn): capacity turns routing into a
+// fixed [N, C, d] buffer (section on where capacity comes from), and the
+// overflow section plus the token-path flowchart (nodes D -> F): once every
+// score is known, an over-full expert keeps its highest-weight tokens.
+//
+// Token order:   slot(t) = #{t' < t : e(t') = e(t)}; kept iff slot < C.
+//   The router already produced, per CTA of 32 tokens, an expert histogram
+//   and each token's rank inside its CTA; scan_kernel turns the histograms
+//   into per-expert exclusive prefixes over CTAs (one CTA per expert), so
+//   slot = prefix[cta(t)][e] + rank(t) -- integer work, bit-exact.
+// Gate priority: tokens of one expert ordered by (gate desc, token asc);
+//   slot = rank in that order; kept iff rank < C.  One CTA per expert sorts
+//   the 64-bit keys (~gate_bits << 32 | token) in shared memory; experts
+//   with more tokens than fit first radix-select the C-th smallest key.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace smoe {
+namespace {
+
+constexpr int kScanThreads = 256;
+
+// Exclusive scan of one int per thread across the block (kScanThreads).
+__device__ int block_exclusive_scan(int v, int* total, int* sh /*[32]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    int o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) sh[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = (lane < (int)(blockDim.x >> 5)) ? sh[lane] : 0;
+    int winc = w;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      int o = __shfl_up_sync(0xffffffffu, winc, off);
+      if (lane >= off) winc += o;
+    }
+    sh[lane] = winc - w;             // exclusive prefix of warp sums
+    if (lane == 31) sh[32] = winc;   // block total
+  }
+  __syncthreads();
+  int res = sh[warp] + inc - v;
+  *total = sh[32];
+  __syncthreads();
+  return res;
+}
+
+// Fixed-shape tree sum (reproducible run to run).
+template <typename F>
+__device__ F block_sum(F v, F* sh /*[32]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off);
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  F r = 0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r += sh[w];
+  __syncthreads();
+  return r;   // valid in thread 0
+}
+
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
+  __shared__ int sh_i[33];
+  __shared__ float sh_f[32];
+  __shared__ double sh_d[32];
+  __shared__ int is_last;
+  const int e = blockIdx.x, tid = threadIdx.x;
+  const int per = (a.R + kScanThreads - 1) / kScanThreads;
+  const int r0 = min(a.R, tid * per), r1 = min(a.R, r0 + per);
+  int cnt = 0;
+  float ps = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    cnt += a.hist[(size_t)r * a.N + e];
+    ps += a.P_part[(size_t)r * a.N + e];
+  }
+  int total;
+  int run = block_exclusive_scan(cnt, &total, sh_i);
+  for (int r = r0; r < r1; ++r) {
+    const size_t i = (size_t)r * a.N + e;
+    const int v = a.hist[i];
+    a.hist[i] = run;
+    run += v;
+  }
+  const float psum = block_sum<float>(ps, sh_f);
+  if (tid == 0) {
+    a.counts[e] = total;
+    a.P_sum[e] = psum;
+    __threadfence();
+    is_last = (atomicAdd(&a.ctrl[0], 1) == a.N - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  // ---- last CTA: prefix of counts, L_aux, GEMM work items -------------
+  // Each thread owns a contiguous run of up to 4 experts.
+  const int per_e = (a.N + kScanThreads - 1) / kScanThreads;   // <= 4 for N <= 1024
+  const int e0 = min(a.N, tid * per_e), e1 = min(a.N, e0 + per_e);
+  int c_loc = 0, t_loc = 0;
+  double aux_loc = 0.0;
+  for (int i = e0; i < e1; ++i) {
+    const int c = __ldcg(a.counts + i);
+    const float p = __ldcg(a.P_sum + i);
+    c_loc += c;
+    t_loc += (min(c, a.C) + a.BN - 1) / a.BN;
+    aux_loc += (double)c * (double)p;
+  }
+  int c_tot, t_tot;
+  int c_run = block_exclusive_scan(c_loc, &c_tot, sh_i);
+  int t_run = block_exclusive_scan(t_loc, &t_tot, sh_i);
+  for (int i = e0; i < e1; ++i) {
+    const int c = __ldcg(a.counts + i);
+    a.expert_start[i] = c_run;
+    c_run += c;
+    const int nt = (min(c, a.C) + a.BN - 1) / a.BN;
+    for (int j = 0; j < nt; ++j) a.entries[t_run + j] = make_int2(i, j);
+    t_run += nt;
+  }
+  const double aux = block_sum<double>(aux_loc, sh_d);
+  if (tid == 0) {
+    a.expert_start[a.N] = c_tot;
+    a.ctrl[1] = t_tot;
+    const double T = (double)a.T;
+    a.aux_loss[0] = (float)((double)a.N * aux / (T * T));  // N * sum (c_i / T)(P_i / T)
+    a.ctrl[0] = 0;
+  }
+}
+
+// Copy one row of `bytes` (a multiple of 16) with the lanes of a warp.
+__device__ __forceinline__ void copy_row(const void* __restrict__ src, void* __restrict__ dst,
+                                         int bytes, int lane) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  const int nv = bytes >> 4;
+  int v = lane;
+  for (; v + 64 <= nv; v += 96) {   // three independent 16-byte loads in flight per lane
+    uint4 a0 = __ldg(s + v), a1 = __ldg(s + v + 32), a2 = __ldg(s + v + 64);
+    d[v] = a0; d[v + 32] = a1; d[v + 64] = a2;
+  }
+  for (; v < nv; v += 32) d[v] = __ldg(s + v);
+}
+
+constexpr int kRowWarps = 8;   // tokens per CTA in the per-token kernels
+
+__global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRowWarps + warp;
+  if (t >= a.T) return;
+  const int e = a.expert_id[t];
+  const int s = a.bases[(size_t)(t / kRouterTM) * a.N + e] + a.local_rank[t];
+  if (a.mode == SWITCH_MOE_TOKEN_ORDER) {
+    const bool kept = s < a.C;
+    if (lane == 0) {
+      a.slot[t] = kept ? s : -1;
+      a.drop[t] = kept ? 0 : 1;
+    }
+    if (kept) {
+      const size_t rb = (size_t)a.d * a.elem_bytes;
+      copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
+               static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
+    }
+  } else if (lane == 0) {
+    a.sorted_list[a.expert_start[e] + s] = t;
+  }
+}
+
+__global__ void __launch_bounds__(kRowWarps * 32) dispatch_kernel(AssignArgs a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kRowWarps + warp;
+  if (t >= a.T) return;
+  const int s = a.slot[t];
+  if (s < 0) return;
+  const int e = a.expert_id[t];
+  const size_t rb = (size_t)a.d * a.elem_bytes;
+  copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
+           static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
+}
+
+constexpr int kSelThreads = 1024;
+
+__device__ __forceinline__ unsigned long long gate_key(const AssignArgs& a, int t) {
+  // gates are positive, so their bit patterns order like their values;
+  // ascending key = descending gate, then ascending token
+  const unsigned g = __float_as_uint(a.gate[t]);
+  return ((unsigned long long)(~g) << 32) | (unsigned)t;
+}
+
+__device__ void bitonic_sort_asc(unsigned long long* k, int P) {
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int j = size >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < P; i += blockDim.x) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const unsigned long long x = k[i], y = k[ixj];
+          const bool up = (i & size) == 0;
+          if ((x > y) == up) { k[i] = y; k[ixj] = x; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSelThreads) gate_select_kernel(AssignArgs a) {
+  extern __shared__ unsigned long long sk[];   // [kGateSortMax]
+  __shared__ int hist[256];
+  __shared__ unsigned long long s_prefix, s_mask;
+  __shared__ int s_krem, s_cnt;
+  const int e = blockIdx.x, tid = threadIdx.x;
+  const int n = a.counts[e];
+  if (n == 0) return;
+  const int32_t* list = a.sorted_list + a.expert_start[e];
+  if (n <= kGateSortMax) {
+    int P = 1;
+    while (P < n) P <<= 1;
+    for (int i = tid; i < P; i += kSelThreads) sk[i] = (i < n) ? gate_key(a, list[i]) : ~0ull;
+    __syncthreads();
+    bitonic_sort_asc(sk, P);
+    for (int i = tid; i < n; i += kSelThreads) {
+      const int t = (int)(unsigned)(sk[i] & 0xffffffffull);
+      const bool kept = i < a.C;
+      a.slot[t] = kept ? i : -1;
+      a.drop[t] = kept ? 0 : 1;
+    }
+    return;
+  }
+  // More tokens than fit: find the C-th smallest key by MSB-first radix
+  // select (keys are unique), keep the keys at or below it, sort those.
+  if (tid == 0) { s_prefix = 0ull; s_mask = 0ull; s_krem = a.C; }
+  __syncthreads();
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+    __syncthreads();
+    const unsigned long long pre = s_prefix, msk = s_mask;
+    for (int i = tid; i < n; i += kSelThreads) {
+      const unsigned long long k = gate_key(a, list[i]);
+      if ((k & msk) == pre) atomicAdd(&hist[(int)((k >> shift) & 255ull)], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int cum = 0, dg = 0;
+      for (; dg < 255; ++dg) {
+        if (cum + hist[dg] >= s_krem) break;
+        cum += hist[dg];
+      }
+      s_krem -= cum;
+      s_prefix = pre | ((unsigned long long)dg << shift);
+      s_mask = msk | (255ull << shift);
+    }
+    __syncthreads();
+  }
+  const unsigned long long thr = s_prefix;
+  if (tid == 0) s_cnt = 0;
+  __syncthreads();
+  for (int i = tid; i < n; i += kSelThreads) {
+    const unsigned long long k = gate_key(a, list[i]);
+    if (k <= thr) {
+      const int pos = atomicAdd(&s_cnt, 1);
+      if (pos < kGateSortMax) sk[pos] = k;
+    } else {
+      const int t = list[i];
+      a.slot[t] = -1;
+      a.drop[t] = 1;
+    }
+  }
+  __syncthreads();
+  const int kept_n = min(s_cnt, kGateSortMax);   // == C
+  int P = 1;
+  while (P < kept_n) P <<= 1;
+  for (int i = kept_n + tid; i < P; i += kSelThreads) sk[i] = ~0ull;
+  __syncthreads();
+  bitonic_sort_asc(sk, P);
+  for (int i = tid; i < kept_n; i += kSelThreads) {
+    const int t = (int)(unsigned)(sk[i] & 0xffffffffull);
+    a.slot[t] = i;
+    a.drop[t] = 0;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s) {
+  scan_kernel<<<a.N, kScanThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_assign(const AssignArgs& a, cudaStream_t s) {
+  assign_kernel<<<(a.T + kRowWarps - 1) / kRowWarps, kRowWarps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s) {
+  dispatch_kernel<<<(a.T + kRowWarps - 1) / kRowWarps, kRowWarps * 32, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s) {
+  const size_t smem = (size_t)kGateSortMax * sizeof(unsigned long long);
+  cudaError_t err = cudaFuncSetAttribute(gate_select_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  gate_select_kernel<<<a.N, kSelThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace smoe

@@ -1,0 +1,131 @@
+// Internal declarations shared by the library's translation units: kernel
+// argument structs and host-side launchers.  Nothing here is exported.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "switch_moe.h"
+
+namespace smoe {
+
+constexpr int kRouterTM = 32;        // tokens per router CTA
+constexpr int kMaxExperts = 1024;
+constexpr int kGateSortMax = 16384;  // keys one gate-priority CTA sorts in shared memory
+constexpr int kTileM = 128;          // weight rows per tensor-core tile (MMA M)
+constexpr int kTileK = 64;           // bf16 elements per 128-byte K block
+constexpr int kSimtTileN = 32;       // tokens per fp32 SIMT tile
+
+// ------------------------------------------------------------------ router
+struct RouterArgs {
+  const void* x;          // [T, d] fp32 or bf16 (ignored when logits_in is set)
+  const float* W_g;       // [N, d]
+  const float* b_g;       // [N] or null
+  const float* logits_in; // [T, N] or null: route these logits instead of x W_g^T
+  float* logits_out;      // [T, N] or null: only compute and store the logits
+  int T, d, N;
+  int x_is_bf16;
+  // routing outputs
+  int32_t* expert_id;     // [T]
+  float* gate;            // [T]
+  float* P_part;          // [R, N]  per-CTA sums of the probabilities
+  int32_t* hist;          // [R, N]  per-CTA expert histograms (scanned in place later)
+  int32_t* local_rank;    // [T]     rank of the token among same-expert tokens of its CTA
+  int32_t* ctrl;          // control words (zeroed by CTA 0)
+};
+cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------- scan / tile lists
+struct ScanArgs {
+  int32_t* hist;          // [R, N] in: histograms; out: exclusive per-expert bases
+  const float* P_part;    // [R, N]
+  int R, N, T, C;
+  int32_t* counts;        // [N] out: expert_counts
+  float* P_sum;           // [N] out: sum over tokens of the probability of expert i
+  int32_t* expert_start;  // [N + 1] out: exclusive prefix of counts
+  float* aux_loss;        // [1] out
+  int2* entries;          // [N * ceil(C / BN)] out: (expert, token tile) work items
+  int BN;                 // token tile of the expert GEMMs
+  int32_t* ctrl;          // ctrl[0] done counter, ctrl[1] number of entries
+};
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
+
+// --------------------------------------------- slots, lists, dispatch
+struct AssignArgs {
+  int T, N, C, d;
+  int elem_bytes;              // 2 (bf16) or 4 (fp32)
+  int mode;                    // SWITCH_MOE_TOKEN_ORDER / SWITCH_MOE_GATE_PRIORITY
+  const int32_t* expert_id;
+  const float* gate;
+  const int32_t* bases;        // [R, N] scanned histograms
+  const int32_t* local_rank;   // [T]
+  const int32_t* counts;       // [N]
+  const int32_t* expert_start; // [N + 1]
+  int32_t* sorted_list;        // [T] tokens grouped by expert, token order within
+  int32_t* slot;               // [T]
+  uint8_t* drop;               // [T]
+  const void* x;               // [T, d]
+  void* xbuf;                  // [N * C, d]
+  int* status;
+};
+// Token order: slot, drop and the dispatch copy in one pass.
+// Gate priority: only the per-expert token lists.
+cudaError_t launch_assign(const AssignArgs& a, cudaStream_t s);
+// Gate priority: per-expert ranking by (gate desc, token asc); slot and drop.
+cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s);
+// Copy kept rows x[t] -> xbuf[e * C + slot[t]] (gate-priority path).
+cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------- expert GEMMs
+// D[e, m, c] = sum_k A[e * M + m, k] * B[e * rows + nt * BN + c, k] for the
+// (expert, token tile) work items; m spans M in 128-row tiles.
+struct GemmArgs {
+  int M, K;                 // rows of A per expert, reduction length
+  int rows_per_expert;      // rows of B (and of the output) per expert
+  int BN;                   // token tile (tensor path: box rows, multiple of 16, <= 256)
+  int m_tiles, k_blocks, ksplit;
+  int num_b;                // 1: B0 only; 2: B0 + B1 (hi + lo halves of a split operand)
+  int stages;
+  const int2* entries;      // work items, or null for one dense problem (e = 0)
+  const int32_t* n_entries; // device count of work items (entries != null)
+  int n_entries_dense;      // count when entries == null
+  const int32_t* counts;    // kept_e = min(counts[e], cap); null: every row kept
+  int cap;
+  int epi;                  // 0: relu -> (bf16 hi, bf16 lo) or fp32; 1: fp32 store
+  void* out0;
+  void* out1;
+  int ldo;                  // output row stride (elements)
+  size_t split_stride;      // elements between the outputs of successive K splits
+  int* status;
+  int grid;
+  size_t smem_bytes;
+};
+// tcgen05 tensor-core path (bf16 operands), TMA-fed.
+cudaError_t launch_gemm_tc(const GemmArgs& g, const CUtensorMap& tmA, const CUtensorMap& tmB0,
+                           const CUtensorMap& tmB1, cudaStream_t s);
+// exact-fp32 path (SIMT FFMA) for dtype fp32; A, B are fp32 device pointers.
+cudaError_t launch_gemm_simt(const GemmArgs& g, const float* A, const float* B, cudaStream_t s);
+int gemm_tc_max_stages(int BN, int num_b);
+size_t gemm_tc_smem_bytes(int BN, int num_b, int stages);
+
+// ------------------------------------------------------- combine
+struct CombineArgs {
+  int T, d, C, ksplit;
+  int gate_multiply;
+  const int32_t* expert_id;
+  const float* gate;
+  const int32_t* slot;
+  const float* O;           // [ksplit][N * C, d] fp32 partial expert outputs
+  size_t split_stride;      // elements between K-split partials
+  const float* S;           // [T, d] shared-expert output or null
+  float* y;                 // [T, d]
+};
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+
+// status word of the current device (see switch_moe_sync_status)
+int* device_status_ptr();
+
+cudaError_t launch_selftest_wait(int* status, unsigned long long timeout_ns, cudaStream_t s);
+
+}  // namespace smoe

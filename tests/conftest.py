@@ -27,4 +27,5 @@ def lib():
     if not gpu_available():
         pytest.skip("no CUDA device")
     import switch_top_expert_router_b300 as sm
+    sm.load_library()   # raises if the CUDA library is missing
     return sm

@@ -1,0 +1,113 @@
+"""Host-side checks of the C ABI (no GPU): the library builds and loads,
+exports every function include/switch_moe.h declares, and its host-only
+functions (capacity, workspace sizing, argument checks) behave."""
+import ctypes
+import math
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "switch_moe.h")
+
+
+@pytest.fixture(scope="module")
+def sm():
+    from switch_top_expert_router_b300 import build
+    build.build()
+    import switch_top_expert_router_b300 as m
+    return m
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(switch_moe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for must in ("switch_moe_forward", "switch_moe_route_from_logits", "switch_moe_capacity",
+                 "switch_moe_workspace_bytes", "switch_moe_sync_status", "switch_moe_strerror"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(sm):
+    lib = ctypes.CDLL(sm.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared but not exported"
+    assert set(declared_functions()) <= set(sm.EXPORTED)
+
+
+def test_capacity_matches_oracle_and_golden(sm):
+    golden = os.path.join(ROOT, "tests", "golden", "capacity.txt")
+    for line in open(golden):
+        line = line.split("#")[0].strip()
+        if line:
+            T, N, cf, C = line.split()
+            assert sm.switch_moe_capacity(int(T), int(N), float(cf)) == int(C)
+    rng = np.random.default_rng(0)
+    for _ in range(5000):
+        T, N = int(rng.integers(1, 1 << 20)), int(rng.integers(1, 1025))
+        cf = float(rng.choice([rng.uniform(0.01, 8.0), 1.0, 1.25, 2.0, 0.1]))
+        assert sm.switch_moe_capacity(T, N, cf) == oracle.capacity(T, N, cf)
+
+
+@pytest.mark.parametrize("T,N,cf", [(0, 4, 1.0), (4, 0, 1.0), (4, 4, 0.0), (4, 4, -2.0),
+                                    (4, 4, math.inf), (4, 4, math.nan)])
+def test_capacity_rejects(sm, T, N, cf):
+    with pytest.raises(sm.SwitchMoEError) as ei:
+        sm.switch_moe_capacity(T, N, cf)
+    assert ei.value.code == sm.SWITCH_MOE_ERR_INVALID_ARG
+
+
+def test_workspace_bytes(sm):
+    p = sm.make_params(8192, 768, 3072, 128, 1.25)
+    base = sm.switch_moe_workspace_bytes(p)
+    # dispatch buffer + H (hi, lo) + O dominate: N*C*(d*2 + 2*F*2 + d*4)
+    NC = 128 * 80
+    assert base >= NC * (768 * 2 + 2 * 3072 * 2 + 768 * 4)
+    assert base < 2 * NC * (768 * 2 + 2 * 3072 * 2 + 768 * 4 * 8) + (1 << 24)
+    bigger = sm.switch_moe_workspace_bytes(sm.make_params(8192, 768, 3072, 128, 2.5))
+    assert bigger > base
+    shared = sm.switch_moe_workspace_bytes(sm.make_params(8192, 768, 3072, 128, 1.25, has_shared=1))
+    assert shared > base
+    hostio = sm.switch_moe_hostio_workspace_bytes(p)
+    assert hostio >= base + 8192 * 768 * (2 + 4)
+    assert sm.switch_moe_workspace_bytes(sm.make_params(0, 768, 3072, 128, 1.25)) >= 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=-1), "INVALID_ARG"), (dict(N=0), "INVALID_ARG"), (dict(d_model=0), "INVALID_ARG"),
+    (dict(capacity_factor=0.0), "INVALID_ARG"), (dict(capacity_factor=float("nan")), "INVALID_ARG"),
+    (dict(priority_mode=2), "INVALID_ARG"), (dict(gate_multiply=3), "INVALID_ARG"),
+    (dict(dtype=5), "INVALID_ARG"), (dict(has_shared=2), "INVALID_ARG"),
+    (dict(N=1025), "UNSUPPORTED"), (dict(d_model=100), "UNSUPPORTED"), (dict(d_ff=12), "UNSUPPORTED"),
+    (dict(T=20000, N=1, capacity_factor=1.0, priority_mode=1), "UNSUPPORTED"),
+])
+def test_workspace_bytes_rejects(sm, kw, code):
+    args = dict(T=1000, d_model=64, d_ff=128, N=8, capacity_factor=1.0, priority_mode=0,
+                gate_multiply=1, dtype=1, has_shared=0)
+    args.update(kw)
+    p = sm.make_params(**args)
+    with pytest.raises(sm.SwitchMoEError) as ei:
+        sm.switch_moe_workspace_bytes(p)
+    assert ei.value.code == getattr(sm, "SWITCH_MOE_ERR_" + code)
+
+
+def test_gate_priority_large_batch_small_capacity_is_supported(sm):
+    # more tokens than one shared-memory sort holds, but C fits: radix-select path
+    p = sm.make_params(20000, 64, 128, 1, 0.5, priority_mode=1)
+    assert sm.switch_moe_workspace_bytes(p) > 0
+
+
+def test_strerror_and_version(sm):
+    assert sm.strerror(0) == "ok"
+    for c in range(-7, 0):
+        assert sm.strerror(c) not in ("ok", "unknown status code")
+    assert sm.strerror(-99) == "unknown status code"
+    assert sm.switch_moe_version() >= 100
