@@ -150,6 +150,29 @@ int switch_moe_route_from_logits(const switch_moe_params* p, const float* logits
                                  float* aux_loss, void* workspace,
                                  size_t workspace_bytes, switch_moe_stream_t stream);
 
+/* switch_moe_route_from_logits() for callers that cannot allocate device
+ * memory when they route: for example a server that gave all of its device
+ * memory to a pool at start-up and allows no cudaMalloc afterwards, or a
+ * runtime with a memory budget fixed before the first request.  There is no
+ * workspace argument; the scratch lives in a static device array of about
+ * 1.2 MiB that every GPU loading the library holds until the process exits.
+ * (The pages have no counterpart to this entry point; it is an interface
+ * convenience of this library.)
+ *   Limits: p->T <= 16384 tokens and p->N <= 256 experts; larger sizes
+ *   return SWITCH_MOE_ERR_UNSUPPORTED and enqueue nothing.
+ *   The first call on a device looks up the array's device address (once
+ *   per device, with that device current); make that first call before any
+ *   stream capture.
+ *   Every call uses the same array: calls that overlap on the GPU (other
+ *   streams, other host threads on the same device) race and must not be
+ *   issued; calls on one stream are ordered and safe.  Nothing left from an
+ *   earlier call is read.
+ *   Outputs and their meaning are those of switch_moe_route_from_logits(). */
+int switch_moe_route_from_logits_noalloc(const switch_moe_params* p, const float* logits,
+                                         int32_t* expert_id, float* gate, int32_t* slot,
+                                         uint8_t* drop_mask, int32_t* expert_counts,
+                                         float* aux_loss, switch_moe_stream_t stream);
+
 /* Step 1 alone: logits [T, N] fp32 = x W_g^T (+ b_g), computed by the same
  * device code that switch_moe_forward() fuses with steps 2-4, so feeding
  * these logits to switch_moe_route_from_logits() reproduces the forward

@@ -48,6 +48,7 @@ EXPORTED = (
     "switch_moe_hostio_workspace_bytes", "switch_moe_forward_hostio",
     "switch_moe_sync_status", "switch_moe_strerror", "switch_moe_version",
     "switch_moe_selftest_wait_timeout", "switch_moe_set_phase_events",
+    "switch_moe_route_from_logits_noalloc",
 )
 NUM_PHASE_EVENTS = 8
 PHASES = ("router", "scan_aux", "slots_dispatch", "expert_gemm1", "shared_gemms",
@@ -90,6 +91,8 @@ def _load() -> ctypes.CDLL:
     lib.switch_moe_forward_hostio.restype = I32
     lib.switch_moe_route_from_logits.argtypes = [P, V, V, V, V, V, V, V, V, ctypes.c_size_t, V]
     lib.switch_moe_route_from_logits.restype = I32
+    lib.switch_moe_route_from_logits_noalloc.argtypes = [P, V, V, V, V, V, V, V, V]
+    lib.switch_moe_route_from_logits_noalloc.restype = I32
     lib.switch_moe_router_logits.argtypes = [P, V, V, V, V, V]
     lib.switch_moe_router_logits.restype = I32
     lib.switch_moe_sync_status.argtypes = [V]
@@ -341,6 +344,34 @@ def switch_moe_route_from_logits(logits: torch.Tensor, capacity_factor: float,
             ctypes.c_size_t(ws.numel()), _stream(stream))
     _check(rc, "switch_moe_route_from_logits")
     return o
+
+
+def switch_moe_route_from_logits_noalloc(logits: torch.Tensor, capacity_factor: float,
+                                         priority_mode: int = TOKEN_ORDER,
+                                         out: Optional[RouteOut] = None,
+                                         stream=None) -> RouteOut:
+    """Routing on given fp32 logits without a workspace, for callers that
+    cannot allocate device memory at routing time (the library keeps the
+    scratch in a static device array).  At most 16384 tokens and 256
+    experts.  Pass preallocated ``out`` tensors to allocate nothing here
+    either."""
+    dev = logits.device
+    _contig(logits, "logits", torch.float32)
+    T, N = logits.shape
+    p = make_params(T, 8, 8, N, capacity_factor, priority_mode, 1, F32, 0)
+    if out is None:
+        out = RouteOut(torch.empty(T, dtype=torch.int32, device=dev),
+                       torch.empty(T, dtype=torch.float32, device=dev),
+                       torch.empty(T, dtype=torch.int32, device=dev),
+                       torch.empty(T, dtype=torch.uint8, device=dev),
+                       torch.empty(N, dtype=torch.int32, device=dev),
+                       torch.empty(1, dtype=torch.float32, device=dev))
+    with torch.cuda.device(dev):
+        rc = _lib.switch_moe_route_from_logits_noalloc(
+            ctypes.byref(p), _ptr(logits), _ptr(out.expert_id), _ptr(out.gate), _ptr(out.slot),
+            _ptr(out.drop_mask), _ptr(out.expert_counts), _ptr(out.aux_loss), _stream(stream))
+    _check(rc, "switch_moe_route_from_logits_noalloc")
+    return out
 
 
 def switch_moe_router_logits(x: torch.Tensor, W_g: torch.Tensor,
