@@ -146,7 +146,7 @@ __device__ __forceinline__ void copy_row(const void* __restrict__ src, void* __r
   uint4* d = reinterpret_cast<uint4*>(dst);
   const int nv = bytes >> 4;
   int v = lane;
-  for (; v + 64 <= nv; v += 96) {   // three independent 16-byte loads in flight per lane
+  for (; v + 64 < nv; v += 96) {    // three independent 16-byte loads in flight per lane
     uint4 a0 = __ldg(s + v), a1 = __ldg(s + v + 32), a2 = __ldg(s + v + 64);
     d[v] = a0; d[v + 32] = a1; d[v + 64] = a2;
   }
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a) {
       a.slot[t] = kept ? s : -1;
       a.drop[t] = kept ? 0 : 1;
     }
-    if (kept) {
+    if (kept && a.xbuf) {   // no buffer when only routing (route_from_logits)
       const size_t rb = (size_t)a.d * a.elem_bytes;
       copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
                static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
