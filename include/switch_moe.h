@@ -176,9 +176,14 @@ int switch_moe_route_from_logits_noalloc(const switch_moe_params* p, const float
 /* Step 1 alone: logits [T, N] fp32 = x W_g^T (+ b_g), computed by the same
  * device code that switch_moe_forward() fuses with steps 2-4, so feeding
  * these logits to switch_moe_route_from_logits() reproduces the forward
- * pass's routing bit for bit ([SWITCH] selective precision: fp32 router). */
+ * pass's routing bit for bit ([SWITCH] selective precision: fp32 router).
+ * Uses p->T, p->d_model, p->N and p->dtype (the type of x).  workspace: at
+ * least switch_moe_workspace_bytes() of a params struct with the same T,
+ * d_model, N and dtype and d_ff = 8 (bf16 layers keep the split router
+ * weights there). */
 int switch_moe_router_logits(const switch_moe_params* p, const void* x,
                              const float* W_g, const float* b_g, float* logits,
+                             void* workspace, size_t workspace_bytes,
                              switch_moe_stream_t stream);
 
 /* switch_moe_forward() with HOST input and output buffers, for callers whose

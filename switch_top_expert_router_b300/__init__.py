@@ -93,7 +93,7 @@ def _load() -> ctypes.CDLL:
     lib.switch_moe_route_from_logits.restype = I32
     lib.switch_moe_route_from_logits_noalloc.argtypes = [P, V, V, V, V, V, V, V, V]
     lib.switch_moe_route_from_logits_noalloc.restype = I32
-    lib.switch_moe_router_logits.argtypes = [P, V, V, V, V, V]
+    lib.switch_moe_router_logits.argtypes = [P, V, V, V, V, V, ctypes.c_size_t, V]
     lib.switch_moe_router_logits.restype = I32
     lib.switch_moe_sync_status.argtypes = [V]
     lib.switch_moe_sync_status.restype = I32
@@ -384,10 +384,12 @@ def switch_moe_router_logits(x: torch.Tensor, W_g: torch.Tensor,
     T, d = x.shape
     N = W_g.shape[0]
     p = make_params(T, d, 8, N, 1.0, TOKEN_ORDER, 1, _dtype_code(x), 0)
+    ws = workspace(switch_moe_workspace_bytes(p), dev)
     logits = torch.empty((T, N), dtype=torch.float32, device=dev)
     with torch.cuda.device(dev):
         rc = _lib.switch_moe_router_logits(ctypes.byref(p), _ptr(x), _ptr(W_g), _ptr(b_g),
-                                           _ptr(logits), _stream(stream))
+                                           _ptr(logits), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                                           _stream(stream))
     _check(rc, "switch_moe_router_logits")
     return logits
 

@@ -100,8 +100,9 @@ struct Plan {
   int max_entries;   // N * ceil(C / BN)
   int ksplit;        // K splits of the second routed GEMM
   // workspace offsets
-  size_t o_Ppart, o_hist, o_rank, o_Psum, o_start, o_list, o_entries, o_ctrl, o_xbuf, o_H0, o_H1,
-      o_O, o_Hs0, o_Hs1, o_Os, total;
+  bool tc_router;    // bf16 x and N <= kMaxExpertsTc: tensor-core router
+  size_t o_Ppart, o_hist, o_rank, o_Psum, o_start, o_list, o_entries, o_ctrl, o_wsplit, o_xbuf,
+      o_H0, o_H1, o_O, o_Hs0, o_Hs1, o_Os, total;
   // extra for the host-IO entry point
   size_t o_xin, o_y, o_eid, o_gate, o_slot, o_drop, o_cnt, o_aux, total_hostio;
 };
@@ -175,6 +176,8 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   q.o_list = take((size_t)q.T * 4);
   q.o_entries = take((size_t)q.max_entries * 8);
   q.o_ctrl = take(64);
+  q.tc_router = q.bf16 && q.N <= kMaxExpertsTc;
+  if (q.tc_router) q.o_wsplit = take((size_t)3 * router_tc_n_mma((int)q.N) * q.d * 2);
   if (need_gemm) {
     q.o_xbuf = take((size_t)NC * q.d * q.elem);
     if (q.bf16) {
@@ -221,6 +224,21 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
+// bf16 router on the tensor cores: split W_g into three bf16 pieces, then
+// logits + softmax/top-1/gate/partials in one kernel.
+int launch_tc_router(const Plan& q, const RouterArgs& ra, void* ws, int* status, cudaStream_t s) {
+  const int n_mma = router_tc_n_mma((int)q.N);
+  __nv_bfloat16* pieces = at<__nv_bfloat16>(ws, q.o_wsplit);
+  if (launch_split_wg(ra.W_g, pieces, (int)q.N, (int)q.d, s) != cudaSuccess)
+    return SWITCH_MOE_ERR_CUDA;
+  CUtensorMap tx, tw;
+  if (!make_map(&tx, ra.x, (uint64_t)q.T, (uint64_t)q.d, 128) ||
+      !make_map(&tw, pieces, (uint64_t)3 * n_mma, (uint64_t)q.d, (uint32_t)n_mma))
+    return SWITCH_MOE_ERR_CUDA;
+  if (launch_router_tc(ra, tx, tw, status, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  return SWITCH_MOE_OK;
+}
+
 // Routing: router -> scan -> slot assignment (-> gate ranking -> dispatch).
 // x == nullptr routes `logits` instead of computing them.
 int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g,
@@ -235,7 +253,12 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   ra.P_part = at<float>(ws, q.o_Ppart); ra.hist = at<int32_t>(ws, q.o_hist);
   ra.local_rank = at<int32_t>(ws, q.o_rank); ra.ctrl = ctrl;
   mark(0, s);
-  if (launch_router(ra, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  if (x && q.tc_router) {
+    int rc = launch_tc_router(q, ra, ws, status, s);
+    if (rc) return rc;
+  } else if (launch_router(ra, s) != cudaSuccess) {
+    return SWITCH_MOE_ERR_CUDA;
+  }
   mark(1, s);
 
   ScanArgs sa{};
@@ -510,22 +533,26 @@ int switch_moe_route_from_logits(const switch_moe_params* p, const float* logits
 }
 
 int switch_moe_router_logits(const switch_moe_params* p, const void* x, const float* W_g,
-                             const float* b_g, float* logits, switch_moe_stream_t stream) {
+                             const float* b_g, float* logits, void* workspace,
+                             size_t workspace_bytes, switch_moe_stream_t stream) {
   Plan q;
   int rc = make_plan(p, &q, false);
   if (rc) return rc;
   const DeviceInfo* dev = current_device();
   if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
   if (q.T == 0) return SWITCH_MOE_OK;
-  if (!x || !W_g || !logits) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (!x || !W_g || !logits || !workspace) return SWITCH_MOE_ERR_INVALID_ARG;
   if (q.d % 8) return SWITCH_MOE_ERR_UNSUPPORTED;
-  if (!al(x, 16) || !al(W_g, 16) || !al(logits, 4) || (b_g && !al(b_g, 4)))
+  if (!al(x, 16) || !al(W_g, 16) || !al(logits, 4) || (b_g && !al(b_g, 4)) ||
+      !al(workspace, 256))
     return SWITCH_MOE_ERR_ALIGNMENT;
+  if (workspace_bytes < q.total) return SWITCH_MOE_ERR_WORKSPACE_TOO_SMALL;
   RouterArgs ra{};
   ra.x = x; ra.W_g = W_g; ra.b_g = b_g; ra.logits_out = logits;
   ra.T = (int)q.T; ra.d = (int)q.d; ra.N = (int)q.N; ra.x_is_bf16 = q.bf16;
-  if (launch_router(ra, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return SWITCH_MOE_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (q.tc_router) return launch_tc_router(q, ra, workspace, dev->status, s);
+  if (launch_router(ra, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   return SWITCH_MOE_OK;
 }
 

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "switch_moe.h"
@@ -16,6 +17,7 @@ constexpr int kGateSortMax = 16384;  // keys one gate-priority CTA sorts in shar
 constexpr int kTileM = 128;          // weight rows per tensor-core tile (MMA M)
 constexpr int kTileK = 64;           // bf16 elements per 128-byte K block
 constexpr int kSimtTileN = 32;       // tokens per fp32 SIMT tile
+constexpr int kMaxExpertsTc = 256;   // experts the tensor-core router takes (one MMA N)
 
 // ------------------------------------------------------------------ router
 struct RouterArgs {
@@ -35,6 +37,13 @@ struct RouterArgs {
   int32_t* ctrl;          // control words (zeroed by CTA 0)
 };
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
+// bf16 layers with N <= kMaxExpertsTc: W_g split into three bf16 pieces
+// [3][n_mma][d] (rows >= N zero), then the tensor-core router over them.
+int router_tc_n_mma(int N);
+cudaError_t launch_split_wg(const float* W_g, __nv_bfloat16* pieces, int N, int d,
+                            cudaStream_t s);
+cudaError_t launch_router_tc(const RouterArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                             int* status, cudaStream_t s);
 
 // ------------------------------------------------------- scan / tile lists
 struct ScanArgs {

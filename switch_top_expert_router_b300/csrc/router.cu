@@ -100,39 +100,30 @@ __device__ void logits_tile(const XT* __restrict__ x, const float* __restrict__ 
 }
 
 // Softmax / argmax / gate / P partials / histogram / in-CTA rank on lg.
+// One thread per token runs the row in increasing expert order (the same
+// operation sequence as the tensor-core router's epilogue, so both give
+// bit-identical results on identical logits):
+//   m = max_i l_i, e = first i with l_i == m (lowest index wins ties),
+//   s = sum_i exp(l_i - m) (sequential), gate = 1 / s, p_i = exp(l_i - m) / s.
 __device__ void route_tile(float* lg, int ldl, int T, int N, int t0, int cta,
                            const RouterArgs& a, int* es, int* hs) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int r = warp; r < TM; r += NTHREADS / 32) {
-    const int t = t0 + r;
-    if (t >= T) continue;                       // warp-uniform
-    float* row = lg + r * ldl;
-    // argmax with the lowest index winning ties: each lane scans i = lane,
-    // lane + 32, ... (increasing), then the warp keeps (larger value, or
-    // equal value with smaller index).
+  if (tid < TM && t0 + tid < T) {
+    const int t = t0 + tid;
+    float* row = lg + tid * ldl;
     float m = -INFINITY;
-    int mi = 0x7fffffff;
-    for (int i = lane; i < N; i += 32) {
-      float v = row[i];
+    int mi = 0;   // stays 0 only if every logit is NaN: keeps the index in range
+    for (int i = 0; i < N; ++i) {
+      const float v = row[i];
       if (v > m) { m = v; mi = i; }
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      float om = __shfl_xor_sync(0xffffffffu, m, off);
-      int oi = __shfl_xor_sync(0xffffffffu, mi, off);
-      if (om > m || (om == m && oi < mi)) { m = om; mi = oi; }
-    }
     float s = 0.f;
-    for (int i = lane; i < N; i += 32) s += expf(row[i] - m);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    for (int i = 0; i < N; ++i) s += expf(row[i] - m);
     const float inv = 1.0f / s;
-    for (int i = lane; i < N; i += 32) row[i] = expf(row[i] - m) * inv;  // probabilities
-    if (lane == 0) {
-      a.expert_id[t] = mi;
-      a.gate[t] = inv;    // score of the argmax: exp(0) / s
-      es[r] = mi;
-    }
+    for (int i = 0; i < N; ++i) row[i] = expf(row[i] - m) * inv;   // probabilities
+    a.expert_id[t] = mi;
+    a.gate[t] = inv;    // score of the argmax: exp(0) / s
+    es[tid] = mi;
   }
   for (int i = tid; i < N; i += NTHREADS) hs[i] = 0;
   __syncthreads();

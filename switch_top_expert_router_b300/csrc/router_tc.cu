@@ -1,0 +1,367 @@
+// Router logits on the tcgen05 tensor cores for bf16 layers, fused with the
+// softmax / top-1 / gate / P-partial / histogram epilogue.
+//
+// Sources: "Top-1 路由 (Top-1 Routing)" (compassingai.com), core mechanism
+// steps 1-2 (score = softmax(W_g x); expert_id = argmax; gate_value =
+// score[expert_id]); Switch Transformer walk-through
+// (personwebsite.pages.dev/moe-switch), selective-precision section: the
+// router computes in float32 although activations are bf16.
+//
+// Exactness.  x is bf16.  The fp32 router weights are split once per call
+// into three bf16 pieces, W_g = W_hi + W_mid + W_lo: each piece is the
+// bf16 rounding of what the previous ones left, every residual is exact in
+// fp32, and the three pieces carry about 24 significant bits (the pieces'
+// sum equals W_g to within 2^-26 relative).  Every product of a bf16 x and a
+// bf16 piece is exact in fp32, so three bf16 MMAs accumulating in fp32
+// give fp32-router logits.  (Plain TF32 or one bf16 copy of W_g would move
+// the logits by ~1e-4, far past the 1e-5 routing-margin rule.)
+//
+// Promotion.  The tensor core's fp32 accumulation loses precision over long
+// chains (measured on B300: logit error std 1.4e-6 at d_model 768 and 2.5e-5
+// at 5120 when all of K accumulates in TMEM, against 2.7e-7 / 1.8e-6 for
+// sequential FFMA).  So each 64-wide K block (4 k-steps x 3 pieces = 12
+// MMAs) accumulates into a fresh TMEM accumulator, and the epilogue warps
+// add that block sum into an fp32 running sum kept in TMEM -- exact fp32
+// additions, one per block.  Two block accumulators alternate so the MMAs of
+// block k+1 overlap the promotion of block k (one when 3 x N columns do not
+// fit in TMEM).
+//
+// CTA = 128 tokens (MMA M) x all experts (MMA N = N rounded up to 16,
+// <= 256), K = d_model in 64-wide TMA stages:
+//   warp 0     TMA: x tile [128 x 64] + the three W_g pieces [n x 64]
+//   warp 1     TMEM allocator + MMA issuer (3 MMAs per 16-wide k step)
+//   warps 2-5  promotion of every K block, then the epilogue: one thread
+//              per token, its N logits read from TMEM
+//              in increasing expert order -- the same operation sequence as
+//              the FFMA router's epilogue, so both route identical logits
+//              identically, bit for bit.
+// Outputs per group of 32 tokens (one epilogue warp), the layout the scan
+// expects: expert histogram, each token's rank among earlier same-expert
+// tokens of the group, and the group's sum of probabilities per expert.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace smoe {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint32_t kXBytes = 128u * 128u;   // 128 tokens x 64 bf16
+constexpr size_t kSmemLimit = 232448;
+constexpr size_t kBarrierArea = 256;
+
+__global__ void split_wg_kernel(const float* __restrict__ W_g, __nv_bfloat16* __restrict__ out,
+                                int N, int n_pad, int d) {
+  const size_t total = (size_t)n_pad * d;
+  for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int e = (int)(idx / d);
+    const float w = e < N ? W_g[idx] : 0.f;
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);       // exact
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);     // exact
+    out[idx] = hi;
+    out[total + idx] = mid;
+    out[2 * total + idx] = __float2bfloat16_rn(r2);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                     const RouterArgs a, int n_mma, int k_blocks, int stages, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t w_bytes = (uint32_t)n_mma * 128u;
+  const uint32_t stage_bytes = kXBytes + 3u * w_bytes;
+  uint8_t* tiles = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * stage_bytes);
+  uint64_t* empty = full + stages;
+  uint64_t* tfull = empty + stages;   // [2] block accumulator ready
+  uint64_t* tempty = tfull + 2;       // [2] block accumulator promoted
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* bias_s = reinterpret_cast<float*>(tmem_slot + 4);          // [N]
+  int* cnt_s = reinterpret_cast<int*>(bias_s + kMaxExpertsTc);      // [4][N] per-warp histograms
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = a.N, T = a.T;
+  const int t0 = blockIdx.x * 128;
+  // TMEM: running sum at column 0, block accumulators after it
+  const bool dbl = 3 * n_mma <= 512;
+  const int nacc = dbl ? 2 : 1;
+  uint32_t tmem_cols = 32;
+  while (tmem_cols < (uint32_t)((1 + nacc) * n_mma)) tmem_cols <<= 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    if (blockIdx.x == 0 && a.ctrl) a.ctrl[0] = 0;   // done counter of the scan that follows
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tensormap(&tmX);
+    prefetch_tensormap(&tmW);
+  }
+  for (int i = threadIdx.x; i < N; i += kThreads) bias_s[i] = a.b_g ? a.b_g[i] : 0.f;
+  for (int i = threadIdx.x; i < 4 * N; i += kThreads) cnt_s[i] = 0;
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_x = l2_policy_evict_first();
+      const uint64_t pol_w = l2_policy_evict_last();   // every CTA reads all of W_g
+      int stage = 0;
+      uint32_t phase = 0, issued = 0;
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
+                       SWITCH_MOE_ERR_DEVICE_TIMEOUT))
+          break;
+        uint8_t* st = tiles + (size_t)stage * stage_bytes;
+        mbar_arrive_expect_tx(&full[stage], stage_bytes);
+        const int kx = kb * kTileK;
+        tma_load_2d(st, &tmX, &full[stage], kx, t0, pol_x);
+        for (int pc = 0; pc < 3; ++pc)
+          tma_load_2d(st + kXBytes + pc * w_bytes, &tmW, &full[stage], kx, pc * n_mma, pol_w);
+        ++issued;
+        if (++stage == stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      const uint32_t S = (uint32_t)stages;
+      for (uint32_t s = 0; s < S && s < issued; ++s) {
+        const uint32_t last = s + S * ((issued - 1u - s) / S);
+        const unsigned long long t0ns = globaltimer_ns();
+        while (!mbar_try_wait(&full[s], (last / S) & 1u)) {
+          if (globaltimer_ns() - t0ns > kWaitTimeoutNs) {
+            atomicExch(status, SWITCH_MOE_ERR_DEVICE_TIMEOUT);
+            break;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(128u, (uint32_t)n_mma);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = 0; kb < k_blocks; ++kb) {
+        const int b = dbl ? (kb & 1) : 0;
+        const uint32_t use = dbl ? (uint32_t)(kb >> 1) : (uint32_t)kb;   // earlier uses of b
+        if (!mbar_wait(&tempty[b], (use & 1u) ^ 1u, abort_flag, status,
+                       SWITCH_MOE_ERR_DEVICE_TIMEOUT))
+          break;
+        tc_fence_after();
+        if (!mbar_wait(&full[stage], phase, abort_flag, status, SWITCH_MOE_ERR_DEVICE_TIMEOUT))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)((1 + b) * n_mma);
+        const uint32_t x_addr = smem_u32(tiles + (size_t)stage * stage_bytes);
+        const uint32_t w_addr = x_addr + kXBytes;
+#pragma unroll
+        for (int k = 0; k < kTileK / 16; ++k) {
+          const uint64_t ad = smem_desc_sw128(x_addr + (uint32_t)k * 32u);
+#pragma unroll
+          for (int pc = 0; pc < 3; ++pc)
+            mma_bf16_ss(d_tmem, ad, smem_desc_sw128(w_addr + pc * w_bytes + (uint32_t)k * 32u),
+                        idesc, (k | pc) != 0 ? 1u : 0u);   // fresh sum per K block
+        }
+        mma_commit(&empty[stage]);
+        mma_commit(&tfull[b]);
+        if (++stage == stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      mma_commit(drain);
+      const unsigned long long t0ns = globaltimer_ns();
+      while (!mbar_try_wait(drain, 0u)) {
+        if (globaltimer_ns() - t0ns > kWaitTimeoutNs) {
+          atomicExch(status, SWITCH_MOE_ERR_DEVICE_TIMEOUT);
+          break;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;                  // TMEM lanes / tokens 32q .. 32q + 31
+    const int row = q * 32 + lane;
+    const int t = t0 + row;
+    const bool valid = t < T;
+    const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);   // running sum
+    float v[16];
+    bool ready = true;
+    for (int kb = 0; kb < k_blocks && ready; ++kb) {
+      const int b = dbl ? (kb & 1) : 0;
+      const uint32_t use = dbl ? (uint32_t)(kb >> 1) : (uint32_t)kb;
+      ready = mbar_wait(&tfull[b], use & 1u, abort_flag, status, SWITCH_MOE_ERR_DEVICE_TIMEOUT);
+      if (!__all_sync(0xffffffffu, ready)) {   // leave together: tcgen05.ld is warp-collective
+        ready = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t blk = taddr + (uint32_t)((1 + b) * n_mma);
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        tmem_ld_32x32b_x16(blk + (uint32_t)c0, v);
+        if (kb > 0) {
+          float r[16];
+          tmem_ld_32x32b_x16(taddr + (uint32_t)c0, r);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = r[j] + v[j];
+        }
+        tmem_st_32x32b_x16(taddr + (uint32_t)c0, v);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
+    }
+    if (ready) {
+      tc_fence_after();
+      // pass 1: max and first argmax, increasing expert order
+      float m = -INFINITY;
+      int mi = 0;
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int i = c0 + j;
+          if (i < N) {
+            const float l = v[j] + bias_s[i];
+            if (l > m) { m = l; mi = i; }
+          }
+        }
+      }
+      // pass 2: sum of exp(l - m), sequential
+      float s = 0.f;
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int i = c0 + j;
+          if (i < N) s += expf((v[j] + bias_s[i]) - m);
+        }
+      }
+      const float inv = 1.0f / s;
+      const int g = blockIdx.x * 4 + q;                // 32-token group
+      const bool group_ok = t0 + q * 32 < T;
+      if (!a.logits_out && valid) {
+        a.expert_id[t] = mi;
+        a.gate[t] = inv;
+      }
+      // pass 3, 32 experts at a time: probabilities through this warp's
+      // [32][33] slice of the (now idle) pipeline buffers, then the group's
+      // per-expert sums with the tokens in order (zeros past T change
+      // nothing).  The debug entry point stores the logits instead.
+      float* pw = reinterpret_cast<float*>(tiles) + (size_t)q * 32 * 33;
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        float v2[16];
+        tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
+        tmem_ld_32x32b_x16(taddr + (uint32_t)c0 + 16u, v2);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int i = c0 + j;
+          const float acc = j < 16 ? v[j] : v2[j - 16];
+          if (i < N) {
+            const float l = acc + bias_s[i];
+            if (a.logits_out) {
+              if (valid) a.logits_out[(size_t)t * N + i] = l;
+            } else {
+              pw[lane * 33 + j] = valid ? expf(l - m) * inv : 0.f;
+            }
+          }
+        }
+        __syncwarp();
+        if (!a.logits_out && group_ok && c0 + lane < N) {
+          float acc = 0.f;
+          for (int r = 0; r < 32; ++r) acc += pw[r * 33 + lane];
+          a.P_part[(size_t)g * N + c0 + lane] = acc;
+        }
+        __syncwarp();
+      }
+      if (!a.logits_out && group_ok) {
+        // histogram and rank among earlier same-expert tokens of the group
+        const int e = valid ? mi : -1 - lane;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        int* hs = cnt_s + q * N;
+        if (valid) {
+          const unsigned lt = (1u << lane) - 1u;
+          a.local_rank[t] = __popc(peers & lt);
+          if ((peers & lt) == 0) hs[e] = __popc(peers);
+        }
+        __syncwarp();
+        for (int i = lane; i < N; i += 32) a.hist[(size_t)g * N + i] = hs[i];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, tmem_cols);
+  }
+}
+
+}  // namespace
+
+int router_tc_n_mma(int N) { return (N + 15) / 16 * 16; }
+
+int router_tc_stages(int N, int d) {
+  const size_t stage = kXBytes + 3u * (size_t)router_tc_n_mma(N) * 128u;
+  const size_t fixed = 1024 + kBarrierArea + (size_t)kMaxExpertsTc * 4 * 5;
+  int st = (int)((kSmemLimit - fixed) / stage);
+  const int kb = (d + kTileK - 1) / kTileK;
+  if (st > kb) st = kb;
+  if (st > 8) st = 8;
+  return st < 1 ? 1 : st;   // one stage always holds the epilogue's 4 x 32 x 33 floats
+}
+
+size_t router_tc_smem_bytes(int N, int d) {
+  const size_t stage = kXBytes + 3u * (size_t)router_tc_n_mma(N) * 128u;
+  return (size_t)router_tc_stages(N, d) * stage + 1024 + kBarrierArea +
+         (size_t)kMaxExpertsTc * 4 * 5;
+}
+
+cudaError_t launch_split_wg(const float* W_g, __nv_bfloat16* pieces, int N, int d,
+                            cudaStream_t s) {
+  const int n_pad = router_tc_n_mma(N);
+  const size_t total = (size_t)n_pad * d;
+  int grid = (int)((total + 255) / 256);
+  if (grid > 1184) grid = 1184;
+  split_wg_kernel<<<grid, 256, 0, s>>>(W_g, pieces, N, n_pad, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_tc(const RouterArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
+                             int* status, cudaStream_t s) {
+  const int n_mma = router_tc_n_mma(a.N);
+  const int stages = router_tc_stages(a.N, a.d);
+  const size_t smem = router_tc_smem_bytes(a.N, a.d);
+  cudaError_t err = cudaFuncSetAttribute(router_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  const int grid = (a.T + 127) / 128;
+  router_tc_kernel<<<grid, kThreads, smem, s>>>(tmX, tmW, a, n_mma, (a.d + kTileK - 1) / kTileK,
+                                                 stages, status);
+  return cudaGetLastError();
+}
+
+}  // namespace smoe

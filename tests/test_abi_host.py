@@ -111,3 +111,9 @@ def test_strerror_and_version(sm):
         assert sm.strerror(c) not in ("ok", "unknown status code")
     assert sm.strerror(-99) == "unknown status code"
     assert sm.switch_moe_version() >= 100
+
+
+def test_binding_wraps_every_declared_function(sm):
+    # the Python binding exposes each C entry point under the same name
+    for name in declared_functions():
+        assert callable(getattr(sm, name, None)), f"no Python wrapper for {name}"
