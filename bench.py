@@ -42,9 +42,45 @@ import torch  # noqa: E402
 
 from workloads import CONFIGS, expert_weights, make_inputs, zipf_bias  # noqa: E402
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
+# gemm_tc_kernel, from the ncu capture summarised in profiles/gemm_tc_base.md
+# (mean of GEMM 1 and GEMM 2).  Valid only for the kernel source it was
+# taken on; any other source reports null.
+NCU_TRAFFIC = {
+    "base": {"gemm_tc_sha256": "4fecb544c6a2be62d1972239cfc7e93e6096ad52640a4615b826b0eeda3a5ae3",
+             "bytes_per_launch": (672.7e6 + 751.7e6) / 2},
+}
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 CPU_SAMPLE_EXPERTS = 16
+
+
+def gemm_traffic(config: str):
+    rec = NCU_TRAFFIC.get(config)
+    if not rec:
+        return None
+    import hashlib
+    src = os.path.join(ROOT, "switch_top_expert_router_b300", "csrc", "gemm_tc.cu")
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != rec["gemm_tc_sha256"]:
+            return None
+    return rec["bytes_per_launch"]
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's value (each rank's timed region); the
+    job is as slow as its slowest replica.  Identity without a group."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(T: int, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank processed `steps` batches of T tokens
+    within the (max-over-ranks) `ms` milliseconds."""
+    return T * steps * world / (ms / 1e3)
 
 
 def peaks():
@@ -257,11 +293,8 @@ def main():
     rc = sm.switch_moe_sync_status()
     if rc != 0:
         raise RuntimeError(f"device status after timing: {sm.strerror(rc)}")
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    value = w.T * args.steps * world / (ms / 1e3)
+    ms = max_over_ranks(ms, pg, dev)
+    value = job_tokens_per_s(w.T, args.steps, world, ms)
 
     # ---- per-phase times (same K steps, events at the phase boundaries)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(sm.NUM_PHASE_EVENTS)]
@@ -323,12 +356,8 @@ def main():
             hstep()
         h1.record(stream)
         torch.cuda.synchronize()
-        hms = h0.elapsed_time(h1)
-        if pg:
-            t = torch.tensor([hms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            hms = float(t.item())
-        e2e = {"value": w.T * args.steps * world / (hms / 1e3), "unit": "tokens/s",
+        hms = max_over_ranks(h0.elapsed_time(h1), pg, dev)
+        e2e = {"value": job_tokens_per_s(w.T, args.steps, world, hms), "unit": "tokens/s",
                "h2d_bytes_per_step": w.T * d * eb,
                "d2h_bytes_per_step": w.T * d * 4 + w.T * 13 + w.N * 4 + 4,
                "ms_per_step": hms / args.steps}
@@ -355,7 +384,8 @@ def main():
             "e2e": e2e,
             "roofline": {"kernel": "gemm_tc_kernel (expert GEMM 1 + 2)", "bound": "hbm",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "peak_kind": peak_kind, "traffic": None,
+                         "frac": achieved / hbm, "peak_kind": peak_kind,
+                         "traffic": gemm_traffic(args.config),
                          "algorithmic_bytes_per_launch": (g1_bytes + g2_bytes) / 2},
             "layer_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": 1e3 * ms / args.steps,
                                "frac": t_roof / (ms / args.steps / 1e3),
