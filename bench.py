@@ -67,6 +67,20 @@ def gemm_traffic(config: str):
     return rec["bytes_per_launch"]
 
 
+def gemm2_ksplit(w, C: int) -> int:
+    """K splits of the second routed GEMM, by the library's rule: split the
+    K = d_ff reduction (in powers of two, at most 8) only while there are
+    fewer than two (expert, token tile, 128-row) tiles per SM of a 148-SM
+    B300."""
+    bn = min(-(-C // 16) * 16, 256)
+    tiles = w.N * -(-C // bn) * -(-w.d_model // 128)
+    k_blocks = -(-w.d_ff // 64)
+    s = 1
+    while s < 8 and tiles * s < 2 * 148 and k_blocks % (2 * s) == 0:
+        s *= 2
+    return s
+
+
 def max_over_ranks(value: float, dist, device) -> float:
     """The largest of every rank's value (each rank's timed region); the
     job is as slow as its slowest replica.  Identity without a group."""
@@ -329,7 +343,13 @@ def main():
                    + 2 * active * wbytes_expert + (2 * wbytes_expert if w.has_shared else 0))
     layer_flops = 4.0 * T_kept * d * F + (4.0 * w.T * d * F if w.has_shared else 0.0)
     t_roof = max(layer_flops / (bf16_peak * 1e12), layer_bytes / (hbm * 1e9))
-    launches = 6 + (2 if w.priority_mode else 0) + (2 if w.has_shared else 0)
+    # kernels per forward: [split W_g +] router, scan, slots/dispatch [+ gate
+    # ranking + dispatch], GEMM 1 [+ shared GEMMs], GEMM 2 [+ combine when the
+    # second GEMM's epilogue cannot do it: fp32 layers, K-split GEMM 2]
+    tc_router = w.dtype == "bf16" and w.N <= 256
+    fused = w.dtype == "bf16" and gemm2_ksplit(w, C) == 1
+    launches = ((2 if tc_router else 1) + 2 + (2 if w.priority_mode else 0) + 2
+                + (2 if w.has_shared else 0) + (0 if fused else 1))
 
     # ---- end to end through the host-buffer entry point
     e2e = None

@@ -99,10 +99,12 @@ struct Plan {
   int BN, BNs;       // token tiles: routed experts, shared expert
   int max_entries;   // N * ceil(C / BN)
   int ksplit;        // K splits of the second routed GEMM
+  bool fused;        // combine in the second routed GEMM's epilogue (tensor path, ksplit 1)
+  int part_units;    // tail-split partial tiles of the tensor-core GEMMs
   // workspace offsets
   bool tc_router;    // bf16 x and N <= kMaxExpertsTc: tensor-core router
   size_t o_Ppart, o_hist, o_rank, o_Psum, o_start, o_list, o_entries, o_ctrl, o_wsplit, o_xbuf,
-      o_H0, o_H1, o_O, o_Hs0, o_Hs1, o_Os, total;
+      o_H0, o_H1, o_O, o_Hs0, o_Hs1, o_Os, o_tok, o_part, o_splitcnt, total;
   // extra for the host-IO entry point
   size_t o_xin, o_y, o_eid, o_gate, o_slot, o_drop, o_cnt, o_aux, total_hostio;
 };
@@ -186,7 +188,17 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
     } else {
       q.o_H0 = take((size_t)NC * q.F * 4);
     }
-    q.o_O = take((size_t)q.ksplit * NC * q.d * 4);
+    q.fused = q.bf16 && q.ksplit == 1;
+    if (q.fused) {
+      q.o_tok = take((size_t)NC * 4);
+    } else {
+      q.o_O = take((size_t)q.ksplit * NC * q.d * 4);
+    }
+    if (q.bf16) {
+      q.part_units = kPlanSMs;
+      q.o_part = take((size_t)q.part_units * kTileM * q.BN * 4);
+      q.o_splitcnt = take((size_t)4 * q.part_units * 4);
+    }
     if (q.shared) {
       if (q.bf16) {
         q.o_Hs0 = take((size_t)q.T * q.F * 2);
@@ -194,7 +206,7 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
       } else {
         q.o_Hs0 = take((size_t)q.T * q.F * 4);
       }
-      q.o_Os = take((size_t)q.T * q.d * 4);
+      if (!q.fused) q.o_Os = take((size_t)q.T * q.d * 4);   // fused: the shared expert writes y
     }
   }
   q.total = o;
@@ -241,10 +253,11 @@ int launch_tc_router(const Plan& q, const RouterArgs& ra, void* ws, int* status,
 
 // Routing: router -> scan -> slot assignment (-> gate ranking -> dispatch).
 // x == nullptr routes `logits` instead of computing them.
+// y (forward with the fused combine, no shared expert): zero rows of dropped tokens.
 int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g,
                 const float* logits, int32_t* expert_id, float* gate, int32_t* slot,
                 uint8_t* drop, int32_t* counts, float* aux, void* ws, bool dispatch,
-                int* status, cudaStream_t s) {
+                float* y, int* status, cudaStream_t s) {
   int32_t* ctrl = at<int32_t>(ws, q.o_ctrl);
   RouterArgs ra{};
   ra.x = x; ra.W_g = W_g; ra.b_g = b_g; ra.logits_in = logits; ra.logits_out = nullptr;
@@ -266,6 +279,10 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   sa.C = q.C; sa.counts = counts; sa.P_sum = at<float>(ws, q.o_Psum);
   sa.expert_start = at<int32_t>(ws, q.o_start); sa.aux_loss = aux;
   sa.entries = at<int2>(ws, q.o_entries); sa.BN = q.BN; sa.ctrl = ctrl;
+  if (dispatch && q.part_units) {
+    sa.split_cnt = at<int32_t>(ws, q.o_splitcnt);
+    sa.n_split_cnt = 4 * q.part_units;
+  }
   if (launch_scan(sa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   mark(2, s);
 
@@ -275,6 +292,8 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   aa.local_rank = ra.local_rank; aa.counts = counts; aa.expert_start = sa.expert_start;
   aa.sorted_list = at<int32_t>(ws, q.o_list); aa.slot = slot; aa.drop = drop;
   aa.x = dispatch ? x : nullptr; aa.xbuf = dispatch ? at<void>(ws, q.o_xbuf) : nullptr;
+  aa.tok_of_slot = (dispatch && q.fused) ? at<int32_t>(ws, q.o_tok) : nullptr;
+  aa.y = (dispatch && q.fused && !q.shared) ? y : nullptr;
   aa.status = status;
   if (launch_assign(aa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   if (q.mode == SWITCH_MOE_GATE_PRIORITY) {
@@ -286,9 +305,10 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
 }
 
 // One tensor-core or SIMT GEMM over routed work items or a dense problem.
+// combine (layer 2, routed, fused plan): out0 is y; gate and gate_multiply scale it.
 int run_gemm(const Plan& q, const DeviceInfo* dev, bool dense, int layer, const void* A,
              const void* B0, const void* B1, void* out0, void* out1, const int32_t* counts,
-             void* ws, cudaStream_t s) {
+             const float* gate, void* ws, cudaStream_t s) {
   GemmArgs g{};
   const int64_t M = layer == 1 ? q.F : q.d;
   const int64_t K = layer == 1 ? q.d : q.F;
@@ -304,6 +324,18 @@ int run_gemm(const Plan& q, const DeviceInfo* dev, bool dense, int layer, const 
   g.out0 = out0; g.out1 = out1;
   g.ldo = (int)M;
   g.status = dev->status;
+  if (layer == 2 && !dense && q.fused) {
+    g.epi = 2;
+    g.tok_of_slot = at<int32_t>(ws, q.o_tok);
+    g.gate = gate;
+    g.gate_multiply = q.gm;
+    g.y_acc = q.shared;   // the shared expert's output is already in y
+  }
+  if (!dense && q.part_units) {
+    g.part = at<float>(ws, q.o_part);
+    g.part_units = q.part_units;
+    g.split_cnt = at<int32_t>(ws, q.o_splitcnt);
+  }
   const int64_t n_ent_max = dense ? g.n_entries_dense : q.max_entries;
   if (q.bf16) {
     g.m_tiles = (int)cdiv(M, kTileM);
@@ -348,24 +380,35 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
                    const void* W2s, float* y, int32_t* expert_id, float* gate, int32_t* slot,
                    uint8_t* drop, int32_t* counts, float* aux, void* ws, cudaStream_t s) {
   int rc = run_routing(q, x, W_g, b_g, nullptr, expert_id, gate, slot, drop, counts, aux, ws,
-                       true, dev->status, s);
+                       true, y, dev->status, s);
   if (rc) return rc;
   void* xbuf = at<void>(ws, q.o_xbuf);
   void* H0 = at<void>(ws, q.o_H0);
   void* H1 = q.bf16 ? at<void>(ws, q.o_H1) : nullptr;
-  float* O = at<float>(ws, q.o_O);
-  if ((rc = run_gemm(q, dev, false, 1, W1, xbuf, nullptr, H0, H1, counts, ws, s))) return rc;
+  if ((rc = run_gemm(q, dev, false, 1, W1, xbuf, nullptr, H0, H1, counts, gate, ws, s)))
+    return rc;
   mark(4, s);
   float* Os = nullptr;
   if (q.shared) {
     void* Hs0 = at<void>(ws, q.o_Hs0);
     void* Hs1 = q.bf16 ? at<void>(ws, q.o_Hs1) : nullptr;
-    Os = at<float>(ws, q.o_Os);
-    if ((rc = run_gemm(q, dev, true, 1, W1s, x, nullptr, Hs0, Hs1, nullptr, ws, s))) return rc;
-    if ((rc = run_gemm(q, dev, true, 2, W2s, Hs0, Hs1, Os, nullptr, nullptr, ws, s))) return rc;
+    Os = q.fused ? y : at<float>(ws, q.o_Os);
+    if ((rc = run_gemm(q, dev, true, 1, W1s, x, nullptr, Hs0, Hs1, nullptr, gate, ws, s)))
+      return rc;
+    if ((rc = run_gemm(q, dev, true, 2, W2s, Hs0, Hs1, Os, nullptr, nullptr, gate, ws, s)))
+      return rc;
   }
   mark(5, s);
-  if ((rc = run_gemm(q, dev, false, 2, W2, H0, H1, O, nullptr, counts, ws, s))) return rc;
+  if (q.fused) {
+    // combine runs in the epilogue of the second routed GEMM
+    if ((rc = run_gemm(q, dev, false, 2, W2, H0, H1, y, nullptr, counts, gate, ws, s)))
+      return rc;
+    mark(6, s);
+    mark(7, s);
+    return SWITCH_MOE_OK;
+  }
+  float* O = at<float>(ws, q.o_O);
+  if ((rc = run_gemm(q, dev, false, 2, W2, H0, H1, O, nullptr, counts, gate, ws, s))) return rc;
   mark(6, s);
   CombineArgs ca{};
   ca.T = (int)q.T; ca.d = (int)q.d; ca.C = q.C;
@@ -527,7 +570,7 @@ int switch_moe_route_from_logits(const switch_moe_params* p, const float* logits
   const bool on = t_phase_on;
   t_phase_on = false;   // phase events belong to the forward calls only
   rc = run_routing(q, nullptr, nullptr, nullptr, logits, expert_id, gate, slot, drop_mask,
-                   expert_counts, aux_loss, workspace, false, dev->status, s);
+                   expert_counts, aux_loss, workspace, false, nullptr, dev->status, s);
   t_phase_on = on;
   return rc;
 }

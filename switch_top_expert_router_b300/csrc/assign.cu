@@ -130,6 +130,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     t_run += nt;
   }
   const double aux = block_sum<double>(aux_loc, sh_d);
+  if (a.split_cnt)
+    for (int i = tid; i < a.n_split_cnt; i += kScanThreads) a.split_cnt[i] = 0;
   if (tid == 0) {
     a.expert_start[a.N] = c_tot;
     a.ctrl[1] = t_tot;
@@ -153,6 +155,13 @@ __device__ __forceinline__ void copy_row(const void* __restrict__ src, void* __r
   for (; v < nv; v += 32) d[v] = __ldg(s + v);
 }
 
+// Zero one fp32 row of d (a multiple of 8) values: the MoE-branch output of
+// a dropped token, which skips every expert.
+__device__ __forceinline__ void zero_row(float* row, int d, int lane) {
+  float4* r = reinterpret_cast<float4*>(row);
+  for (int v = lane; v < (d >> 2); v += 32) r[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 constexpr int kRowWarps = 8;   // tokens per CTA in the per-token kernels
 
 __global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a) {
@@ -171,7 +180,9 @@ __global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a) {
       const size_t rb = (size_t)a.d * a.elem_bytes;
       copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
                static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
+      if (a.tok_of_slot && lane == 0) a.tok_of_slot[(size_t)e * a.C + s] = t;
     }
+    if (!kept && a.y) zero_row(a.y + (size_t)t * a.d, a.d, lane);
   } else if (lane == 0) {
     a.sorted_list[a.expert_start[e] + s] = t;
   }
@@ -182,11 +193,15 @@ __global__ void __launch_bounds__(kRowWarps * 32) dispatch_kernel(AssignArgs a) 
   const int t = blockIdx.x * kRowWarps + warp;
   if (t >= a.T) return;
   const int s = a.slot[t];
-  if (s < 0) return;
+  if (s < 0) {
+    if (a.y) zero_row(a.y + (size_t)t * a.d, a.d, lane);
+    return;
+  }
   const int e = a.expert_id[t];
   const size_t rb = (size_t)a.d * a.elem_bytes;
   copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
            static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
+  if (a.tok_of_slot && lane == 0) a.tok_of_slot[(size_t)e * a.C + s] = t;
 }
 
 constexpr int kSelThreads = 1024;

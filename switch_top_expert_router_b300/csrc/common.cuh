@@ -57,6 +57,8 @@ struct ScanArgs {
   int2* entries;          // [N * ceil(C / BN)] out: (expert, token tile) work items
   int BN;                 // token tile of the expert GEMMs
   int32_t* ctrl;          // ctrl[0] done counter, ctrl[1] number of entries
+  int32_t* split_cnt;     // [n_split_cnt] zeroed for the expert GEMMs' tail split, or null
+  int n_split_cnt;
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
 
@@ -76,6 +78,8 @@ struct AssignArgs {
   uint8_t* drop;               // [T]
   const void* x;               // [T, d]
   void* xbuf;                  // [N * C, d]
+  int32_t* tok_of_slot;        // [N * C] token of each filled slot, or null
+  float* y;                    // [T, d] fp32: rows of dropped tokens zeroed, or null
   int* status;
 };
 // Token order: slot, drop and the dispatch copy in one pass.
@@ -101,11 +105,24 @@ struct GemmArgs {
   int n_entries_dense;      // count when entries == null
   const int32_t* counts;    // kept_e = min(counts[e], cap); null: every row kept
   int cap;
-  int epi;                  // 0: relu -> (bf16 hi, bf16 lo) or fp32; 1: fp32 store
-  void* out0;
+  int epi;                  // 0: relu -> (bf16 hi, bf16 lo) or fp32; 1: fp32 store;
+                            // 2: combine (tensor path): y[tok] = g_tok * D (+ y[tok])
+  void* out0;               // epi 2: y [T, M] fp32
   void* out1;
   int ldo;                  // output row stride (elements)
   size_t split_stride;      // elements between the outputs of successive K splits
+  // epi 2: token of every filled slot, gates, scale flag, accumulate into y
+  const int32_t* tok_of_slot;   // [N * C]
+  const float* gate;            // [T]
+  int gate_multiply;
+  int y_acc;
+  // Tensor path, ksplit == 1: when the last wave of tiles is less than half
+  // full, its tiles are cut along K into pieces that run on the idle CTAs;
+  // the pieces leave fp32 partials and the last piece of each 32-row slice
+  // to finish sums them in piece order.  null part: no tail split.
+  float* part;              // [part_units][kTileM * BN]
+  int part_units;
+  int32_t* split_cnt;       // [4 * part_units]: zero on entry, left zero on exit
   int* status;
   int grid;
   size_t smem_bytes;

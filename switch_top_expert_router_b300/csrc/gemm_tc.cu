@@ -16,8 +16,21 @@
 // sees H with ~16 significant bits (a single bf16 rounding of H moves y by
 // more than the 1e-2 * rms(y) budget at these sizes).
 //
-// CTA = 6 warps, persistent over a static round-robin of work tiles
-// (expert, token tile, 128-row weight tile, K split):
+// Second layer of the routed experts: the epilogue is also the combine step
+// -- each filled slot's row goes straight to its token's row of y, scaled by
+// the gate when gate_multiply is set ("Top-1 路由 (Top-1 Routing)", core
+// mechanism step 3, against the Switch Transformer walk-through's Switch
+// layer, Eq. 2), so the expert outputs never round-trip through HBM.
+//
+// Tail split: tiles are handed out round-robin, so when the last wave is
+// less than half full most SMs would idle while a few stream whole weight
+// tiles.  Those last tiles are cut along K into equal pieces run by the idle
+// CTAs; each piece stores its fp32 partial, and for every 32-row slice the
+// last piece to finish (an atomic counter) adds the partials in piece order
+// -- deterministic, whatever the finishing order -- and applies the epilogue.
+//
+// CTA = 6 warps, persistent over a static round-robin of work units
+// (expert, token tile, 128-row weight tile, K range):
 //   warp 0      TMA producer (one lane) into a `stages`-deep shared ring
 //   warp 1      TMEM allocator + MMA issuer (one lane)
 //   warps 2..5  epilogue: TMEM -> registers -> global, 32 TMEM lanes each
@@ -37,6 +50,8 @@ constexpr int kThreads = 192;
 constexpr uint32_t kABytes = kTileM * 128;     // 16 KB per stage
 constexpr size_t kSmemLimit = 232448;          // opt-in dynamic shared memory per block
 constexpr size_t kBarrierArea = 512;
+constexpr int kMaxPieces = 8;          // K pieces per split tile
+constexpr int kMinPieceKBlocks = 4;    // 256 of K at least per piece
 
 __device__ __forceinline__ void decode_tile(const GemmArgs& g, int tile, int& e, int& nt,
                                             int& mt, int& ks, int& nv) {
@@ -55,6 +70,55 @@ __device__ __forceinline__ void decode_tile(const GemmArgs& g, int tile, int& e,
   }
   const int kept = g.counts ? min(g.counts[e], g.cap) : g.rows_per_expert;
   nv = min(g.BN, kept - nt * g.BN);
+}
+
+// Tail split plan for `total` tiles over the grid: tiles [0, full) run whole,
+// the remaining total - full tiles run as `pieces` K pieces each.
+__device__ __forceinline__ void split_plan(const GemmArgs& g, int total, int& full,
+                                           int& pieces) {
+  full = total;
+  pieces = 1;
+  if (!g.part || g.ksplit != 1) return;
+  const int grid = (int)gridDim.x;
+  const int rem = total % grid;
+  if (rem == 0 || 2 * rem > grid) return;
+  int p = grid / rem;
+  p = min(p, g.k_blocks / kMinPieceKBlocks);
+  p = min(p, kMaxPieces);
+  if (p < 2 || rem * p > g.part_units) return;
+  full = total - rem;
+  pieces = p;
+}
+
+struct Work {
+  int e, nt, mt, ks, nv;
+  int kb0, nkb;   // K blocks [kb0, kb0 + nkb)
+  int unit;       // index of the piece among all split pieces, -1: whole tile
+  int sidx;       // index of the split tile
+  int pieces;
+};
+
+__device__ __forceinline__ void decode_work(const GemmArgs& g, int u, int full, int pieces,
+                                            Work& w) {
+  int tile = u;
+  w.unit = -1;
+  w.sidx = 0;
+  w.pieces = pieces;
+  int piece = 0;
+  if (u >= full) {
+    w.unit = u - full;
+    w.sidx = w.unit / pieces;
+    piece = w.unit - w.sidx * pieces;
+    tile = full + w.sidx;
+  }
+  decode_tile(g, tile, w.e, w.nt, w.mt, w.ks, w.nv);
+  if (w.unit < 0) {
+    w.kb0 = w.ks * g.k_blocks;
+    w.nkb = g.k_blocks;
+  } else {
+    w.kb0 = piece * g.k_blocks / pieces;
+    w.nkb = (piece + 1) * g.k_blocks / pieces - w.kb0;
+  }
 }
 
 // Bounded wait that ignores the abort flag: used at teardown to let copies
@@ -119,6 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_entries = g.entries ? *g.n_entries : g.n_entries_dense;
   const int total = n_entries * g.m_tiles * g.ksplit;
+  int full_tiles, pieces;
+  split_plan(g, total, full_tiles, pieces);
+  const int n_units = full_tiles + (total - full_tiles) * pieces;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -128,13 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        int e, nt, mt, ks, nv;
-        decode_tile(g, tile, e, nt, mt, ks, nv);
-        const int ya = e * g.M + mt * kTileM;
-        const int yb = e * g.rows_per_expert + nt * g.BN;
-        const int kb0 = ks * g.k_blocks;
-        for (int kb = 0; kb < g.k_blocks; ++kb) {
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        Work w;
+        decode_work(g, u, full_tiles, pieces, w);
+        const int ya = w.e * g.M + w.mt * kTileM;
+        const int yb = w.e * g.rows_per_expert + w.nt * g.BN;
+        for (int kb = 0; kb < w.nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
                          SWITCH_MOE_ERR_DEVICE_TIMEOUT)) {
             ok = false;
@@ -142,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = tiles + (size_t)stage * stage_bytes;
           mbar_arrive_expect_tx(&full[stage], stage_bytes);
-          const int kx = (kb0 + kb) * kTileK;
+          const int kx = (w.kb0 + kb) * kTileK;
           tma_load_2d(st, &tmA, &full[stage], kx, ya, pol_a);
           tma_load_2d(st + kABytes, &tmB0, &full[stage], kx, yb, pol_b);
           if (g.num_b == 2) tma_load_2d(st + kABytes + b_bytes, &tmB1, &full[stage], kx, yb, pol_b);
@@ -166,9 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int stage = 0;
       uint32_t phase = 0, it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x, ++it) {
-        int e, nt, mt, ks, nv;
-        decode_tile(g, tile, e, nt, mt, ks, nv);
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++it) {
+        Work w;
+        decode_work(g, u, full_tiles, pieces, w);
         const uint32_t acc = it & 1u, acc_par = (it >> 1) & 1u;
         if (!mbar_wait(&tempty[acc], acc_par ^ 1u, abort_flag, status,
                        SWITCH_MOE_ERR_DEVICE_TIMEOUT)) {
@@ -177,9 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * acc_stride;
-        const uint32_t n_mma = ((uint32_t)nv + 15u) & ~15u;
+        const uint32_t n_mma = ((uint32_t)w.nv + 15u) & ~15u;
         const uint32_t idesc = idesc_bf16_f32(128u, n_mma);
-        for (int kb = 0; kb < g.k_blocks; ++kb) {
+        for (int kb = 0; kb < w.nkb; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, status,
                          SWITCH_MOE_ERR_DEVICE_TIMEOUT)) {
             ok = false;
@@ -212,30 +278,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;   // TMEM lanes 32q .. 32q + 31 belong to this warp
+    const unsigned kAll = 0xffffffffu;
     uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      int e, nt, mt, ks, nv;
-      decode_tile(g, tile, e, nt, mt, ks, nv);
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+      Work w;
+      decode_work(g, u, full_tiles, pieces, w);
       const uint32_t acc = it & 1u, acc_par = (it >> 1) & 1u;
+      const int row = w.mt * kTileM + q * 32 + lane;   // weight row = output column
+      const bool row_ok = row < g.M;
+      const size_t out_row0 = (size_t)w.e * g.rows_per_expert + (size_t)w.nt * g.BN;
+      // combine: token and gate of columns c .. c + 31, one column per lane
+      auto tok_gate = [&](int c, int& tk, float& gv) {
+        tk = 0;
+        gv = 1.f;
+        if (c + lane < w.nv) {
+          tk = g.tok_of_slot[out_row0 + (size_t)(c + lane)];
+          if (g.gate_multiply) gv = g.gate[tk];
+        }
+      };
+      int tk32 = 0;
+      float gv32 = 1.f;
+      if (g.epi == 2 && w.unit < 0) tok_gate(0, tk32, gv32);   // overlaps the wait below
       // tcgen05.ld below is warp-collective: leave the loop together or not at all
       const bool ready =
           mbar_wait(&tfull[acc], acc_par, abort_flag, status, SWITCH_MOE_ERR_DEVICE_TIMEOUT);
-      if (!__all_sync(0xffffffffu, ready)) break;
+      if (!__all_sync(kAll, ready)) break;
       tc_fence_after();
-      const int row = mt * kTileM + q * 32 + lane;   // weight row = output column
-      const bool row_ok = row < g.M;
-      const size_t out_row0 = (size_t)e * g.rows_per_expert + (size_t)nt * g.BN;
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * acc_stride;
-      for (int c0 = 0; c0 < nv; c0 += 16) {
-        float v[16];
-        tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
-        if (row_ok) {
+
+      // Stores 16 accumulator columns c0 .. c0 + 15 of this thread's row.
+      auto store_chunk = [&](int c0, const float (&v)[16]) {
+        if (g.epi == 2) {
+          int tk;
+          float gv;
+          tok_gate(c0, tk, gv);   // lanes 16..31 load columns the chunk does not use
+          float* y = static_cast<float*>(g.out0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int tj = __shfl_sync(kAll, tk, j);
+            const float gj = __shfl_sync(kAll, gv, j);
+            if (row_ok && c0 + j < w.nv) {
+              float* dst = y + (size_t)tj * (size_t)g.ldo + row;
+              const float val = gj * v[j];
+              *dst = g.y_acc ? *dst + val : val;
+            }
+          }
+        } else if (row_ok) {
           if (g.epi == 0) {
             __nv_bfloat16* hi = static_cast<__nv_bfloat16*>(g.out0);
             __nv_bfloat16* lo = static_cast<__nv_bfloat16*>(g.out1);
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              if (c0 + j < nv) {
+              if (c0 + j < w.nv) {
                 const size_t o = (out_row0 + (size_t)(c0 + j)) * (size_t)g.ldo + row;
                 const float h = fmaxf(v[j], 0.f);
                 const __nv_bfloat16 bh = __float2bfloat16_rn(h);
@@ -244,17 +338,95 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {
-            float* out = static_cast<float*>(g.out0) + (size_t)ks * g.split_stride;
+            float* out = static_cast<float*>(g.out0) + (size_t)w.ks * g.split_stride;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              if (c0 + j < nv) out[(out_row0 + (size_t)(c0 + j)) * (size_t)g.ldo + row] = v[j];
+              if (c0 + j < w.nv) out[(out_row0 + (size_t)(c0 + j)) * (size_t)g.ldo + row] = v[j];
             }
           }
         }
+      };
+
+      if (w.unit < 0 && g.epi == 2) {
+        float* y = static_cast<float*>(g.out0);
+        for (int c0 = 0; c0 < w.nv; c0 += 32) {
+          if (c0 > 0) tok_gate(c0, tk32, gv32);
+          float v[2][16];
+          tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v[0]);
+          tmem_ld_32x32b_x16(taddr + (uint32_t)c0 + 16u, v[1]);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int tj = __shfl_sync(kAll, tk32, j);
+            const float gj = __shfl_sync(kAll, gv32, j);
+            if (row_ok && c0 + j < w.nv) {
+              float* dst = y + (size_t)tj * (size_t)g.ldo + row;
+              const float val = gj * v[j >> 4][j & 15];
+              *dst = g.y_acc ? *dst + val : val;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      } else if (w.unit < 0) {
+        for (int c0 = 0; c0 < w.nv; c0 += 16) {
+          float v[16];
+          tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
+          store_chunk(c0, v);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+      } else {
+        // one K piece of a split tile: park the partial, [column][128 rows]
+        const size_t tile_elems = (size_t)kTileM * (size_t)g.BN;
+        float* mine = g.part + (size_t)w.unit * tile_elems + q * 32 + lane;
+        for (int c0 = 0; c0 < w.nv; c0 += 16) {
+          float v[16];
+          tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < w.nv) mine[(size_t)(c0 + j) * kTileM] = v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          int32_t* cnt = g.split_cnt + w.sidx * 4 + q;
+          last = atomicAdd(cnt, 1) == w.pieces - 1;
+          if (last) *cnt = 0;   // every piece has arrived: reset for the next launch
+        }
+        last = __shfl_sync(kAll, last, 0);
+        if (last) {
+          __threadfence();
+          const float* p0 = g.part + (size_t)w.sidx * w.pieces * tile_elems + q * 32 + lane;
+          for (int c0 = 0; c0 < w.nv; c0 += 16) {
+            // sum in piece order; four pieces' loads in flight at a time
+            float v[16];
+            for (int p4 = 0; p4 < w.pieces; p4 += 4) {
+              float t[4][16];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float* src = p0 + (size_t)(p4 + i) * tile_elems + (size_t)c0 * kTileM;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  t[i][j] = (p4 + i < w.pieces && c0 + j < w.nv) ? __ldcg(src + j * kTileM) : 0.f;
+              }
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                if (p4 + i < w.pieces) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) v[j] = (p4 + i == 0) ? t[i][j] : v[j] + t[i][j];
+                }
+              }
+            }
+            store_chunk(c0, v);
+          }
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[acc]);
     }
   }
   tc_fence_before();

@@ -68,6 +68,134 @@ __global__ void split_wg_kernel(const float* __restrict__ W_g, __nv_bfloat16* __
   }
 }
 
+constexpr int kRegExperts = 128;   // experts whose running sums fit in registers
+
+// Outputs of one token group (32 tokens = one epilogue warp) from the
+// finished logits: expert id, gate, per-expert probability sums of the
+// group and its histogram plus in-group ranks.  l[] holds the token's
+// logits on entry (bias added); it is overwritten with exp(l - max).
+__device__ __forceinline__ void route_token_regs(const RouterArgs& a, float (&l)[kRegExperts],
+                                                 uint8_t* tiles, int* cnt_s, int q, int lane,
+                                                 int t0, int t, bool valid) {
+  const int N = a.N, T = a.T;
+  if (a.logits_out) {   // debug entry point: the logits only
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < kRegExperts; ++i)
+        if (i < N) a.logits_out[(size_t)t * N + i] = l[i];
+    }
+    return;
+  }
+  // max and first argmax, increasing expert order
+  float m = -INFINITY;
+  int mi = 0;
+#pragma unroll
+  for (int i = 0; i < kRegExperts; ++i) {
+    if (i < N && l[i] > m) {
+      m = l[i];
+      mi = i;
+    }
+  }
+  // sum of exp(l - m), sequential in expert order
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRegExperts; ++i) {
+    if (i < N) {
+      l[i] = expf(l[i] - m);
+      s += l[i];
+    }
+  }
+  const float inv = 1.0f / s;
+  const int g = blockIdx.x * 4 + q;                // 32-token group
+  const bool group_ok = t0 + q * 32 < T;
+  if (valid) {
+    a.expert_id[t] = mi;
+    a.gate[t] = inv;   // exp(0) / s: the probability of the argmax
+  }
+  // Group sums of the probabilities, 32 experts at a time, transposed
+  // through this warp's [32][33] slice of the (now idle) pipeline buffers;
+  // tokens past T contribute zeros.
+  float* pw = reinterpret_cast<float*>(tiles) + (size_t)q * 32 * 33;
+#pragma unroll
+  for (int c0 = 0; c0 < kRegExperts; c0 += 32) {
+    if (c0 < N) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (c0 + j < N) pw[lane * 33 + j] = valid ? l[c0 + j] * inv : 0.f;
+      __syncwarp();
+      if (group_ok && c0 + lane < N) {
+        float acc = 0.f;
+        for (int r = 0; r < 32; ++r) acc += pw[r * 33 + lane];
+        a.P_part[(size_t)g * N + c0 + lane] = acc;
+      }
+      __syncwarp();
+    }
+  }
+  if (group_ok) {
+    // histogram and rank among earlier same-expert tokens of the group
+    const int e = valid ? mi : -1 - lane;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    int* hs = cnt_s + q * N;
+    if (valid) {
+      const unsigned lt = (1u << lane) - 1u;
+      a.local_rank[t] = __popc(peers & lt);
+      if ((peers & lt) == 0) hs[e] = __popc(peers);
+    }
+    __syncwarp();
+    for (int i = lane; i < N; i += 32) a.hist[(size_t)g * N + i] = hs[i];
+  }
+}
+
+// Epilogue warps for N <= kRegExperts: promote every K block's TMEM sum
+// into registers (running[i] += block[i], the same fp32 additions in the
+// same order as the TMEM-resident variant), then route the token.
+__device__ __forceinline__ void router_epilogue_regs(
+    const RouterArgs& a, uint32_t taddr, int n_mma, int k_blocks, bool dbl, uint64_t* tfull,
+    uint64_t* tempty, volatile int* abort_flag, int* status, uint8_t* tiles,
+    const float* bias_s, int* cnt_s, int q, int lane, int t0, int t, bool valid) {
+  const int nch = n_mma >> 4;   // 16-column chunks, <= 8
+  float run[kRegExperts];
+#pragma unroll
+  for (int i = 0; i < kRegExperts; ++i) run[i] = 0.f;
+  for (int kb = 0; kb < k_blocks; ++kb) {
+    const int b = dbl ? (kb & 1) : 0;
+    const uint32_t use = dbl ? (uint32_t)(kb >> 1) : (uint32_t)kb;
+    const bool ready =
+        mbar_wait(&tfull[b], use & 1u, abort_flag, status, SWITCH_MOE_ERR_DEVICE_TIMEOUT);
+    if (!__all_sync(0xffffffffu, ready)) return;   // tcgen05.ld is warp-collective
+    tc_fence_after();
+    const uint32_t blk = taddr + (uint32_t)((1 + b) * n_mma);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {   // 4 chunks (64 columns) in flight at a time
+      uint32_t r[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (h * 4 + c < nch) tmem_ld_32x32b_x16_async(blk + (uint32_t)((h * 4 + c) * 16), r[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (h * 4 + c < nch) {
+          tmem_wait_ld_regs(r[c]);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int i = (h * 4 + c) * 16 + j;
+            run[i] = kb == 0 ? __uint_as_float(r[c][j]) : run[i] + __uint_as_float(r[c][j]);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&tempty[b]);
+  }
+#pragma unroll
+  for (int i = 0; i < kRegExperts; ++i)
+    if (i < a.N) run[i] = run[i] + bias_s[i];
+  route_token_regs(a, run, tiles, cnt_s, q, lane, t0, t, valid);
+}
+
+// kRegs (N <= kRegExperts): each epilogue thread keeps its token's running
+// sums in registers; otherwise they live in TMEM column block 0.
+template <bool kRegs>
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const RouterArgs a, int n_mma, int k_blocks, int stages, int* status) {
@@ -207,6 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = t0 + row;
     const bool valid = t < T;
     const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16);   // running sum
+    if constexpr (kRegs) {
+      router_epilogue_regs(a, taddr, n_mma, k_blocks, dbl, tfull, tempty, abort_flag, status,
+                           tiles, bias_s, cnt_s, q, lane, t0, t, valid);
+    } else {
     float v[16];
     bool ready = true;
     for (int kb = 0; kb < k_blocks && ready; ++kb) {
@@ -311,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = lane; i < N; i += 32) a.hist[(size_t)g * N + i] = hs[i];
       }
     }
+    }   // !kRegs
   }
   tc_fence_before();
   __syncthreads();
@@ -355,12 +488,14 @@ cudaError_t launch_router_tc(const RouterArgs& a, const CUtensorMap& tmX, const 
   const int n_mma = router_tc_n_mma(a.N);
   const int stages = router_tc_stages(a.N, a.d);
   const size_t smem = router_tc_smem_bytes(a.N, a.d);
-  cudaError_t err = cudaFuncSetAttribute(router_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const bool regs = a.N <= kRegExperts;
+  auto kern = regs ? router_tc_kernel<true> : router_tc_kernel<false>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int grid = (a.T + 127) / 128;
-  router_tc_kernel<<<grid, kThreads, smem, s>>>(tmX, tmW, a, n_mma, (a.d + kTileK - 1) / kTileK,
-                                                 stages, status);
+  kern<<<grid, kThreads, smem, s>>>(tmX, tmW, a, n_mma, (a.d + kTileK - 1) / kTileK, stages,
+                                    status);
   return cudaGetLastError();
 }
 

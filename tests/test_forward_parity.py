@@ -48,6 +48,9 @@ SMALL = [
     ("bf16-C1", 400, 64, 128, 4, 0.01, "bf16", 0, 1, 0),          # C = 1
     ("f32-gate-prio-shared", 700, 96, 160, 5, 0.8, "f32", 1, 0, 1),
     ("bf16-big-C", 2000, 64, 256, 2, 1.0, "bf16", 1, 1, 1),       # C = 1000, gate prio, shared
+    # 512 weight tiles per GEMM on a 148-CTA grid: the last 68 run as two K pieces each
+    ("bf16-tail-split", 2048, 1024, 1024, 64, 1.0, "bf16", 0, 1, 0),
+    ("bf16-tail-split-gate-shared", 2048, 1024, 1024, 64, 1.0, "bf16", 1, 0, 1),
 ]
 
 
