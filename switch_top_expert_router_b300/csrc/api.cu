@@ -247,7 +247,7 @@ int launch_tc_router(const Plan& q, const RouterArgs& ra, void* ws, int* status,
   if (!make_map(&tx, ra.x, (uint64_t)q.T, (uint64_t)q.d, 128) ||
       !make_map(&tw, pieces, (uint64_t)3 * n_mma, (uint64_t)q.d, (uint32_t)n_mma))
     return SWITCH_MOE_ERR_CUDA;
-  if (launch_router_tc(ra, tx, tw, status, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  if (launch_router_tc(ra, tx, tw, status, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   return SWITCH_MOE_OK;
 }
 
@@ -283,7 +283,7 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
     sa.split_cnt = at<int32_t>(ws, q.o_splitcnt);
     sa.n_split_cnt = 4 * q.part_units;
   }
-  if (launch_scan(sa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  if (launch_scan(sa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   mark(2, s);
 
   AssignArgs aa{};
@@ -295,10 +295,10 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   aa.tok_of_slot = (dispatch && q.fused) ? at<int32_t>(ws, q.o_tok) : nullptr;
   aa.y = (dispatch && q.fused && !q.shared) ? y : nullptr;
   aa.status = status;
-  if (launch_assign(aa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  if (launch_assign(aa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   if (q.mode == SWITCH_MOE_GATE_PRIORITY) {
-    if (launch_gate_select(aa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
-    if (dispatch && launch_dispatch(aa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+    if (launch_gate_select(aa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+    if (dispatch && launch_dispatch(aa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   }
   mark(3, s);
   return SWITCH_MOE_OK;
@@ -359,7 +359,7 @@ int run_gemm(const Plan& q, const DeviceInfo* dev, bool dense, int layer, const 
     } else {
       tb1 = tb0;
     }
-    if (launch_gemm_tc(g, ta, tb0, tb1, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+    if (launch_gemm_tc(g, ta, tb0, tb1, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   } else {
     g.m_tiles = (int)cdiv(M, 64);
     g.ksplit = 1;
@@ -368,8 +368,8 @@ int run_gemm(const Plan& q, const DeviceInfo* dev, bool dense, int layer, const 
     g.split_stride = (size_t)q.N * q.C * q.d;
     const int64_t tiles_max = n_ent_max * g.m_tiles;
     g.grid = (int)tiles_max;
-    if (launch_gemm_simt(g, static_cast<const float*>(A), static_cast<const float*>(B0), s) !=
-        cudaSuccess)
+    if (launch_gemm_simt(g, static_cast<const float*>(A), static_cast<const float*>(B0), s,
+                         true) != cudaSuccess)
       return SWITCH_MOE_ERR_CUDA;
   }
   return SWITCH_MOE_OK;
@@ -415,7 +415,7 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
   ca.ksplit = q.bf16 ? q.ksplit : 1;
   ca.gate_multiply = q.gm; ca.expert_id = expert_id; ca.gate = gate; ca.slot = slot;
   ca.O = O; ca.split_stride = (size_t)q.N * q.C * q.d; ca.S = Os; ca.y = y;
-  if (launch_combine(ca, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  if (launch_combine(ca, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   mark(7, s);
   return SWITCH_MOE_OK;
 }

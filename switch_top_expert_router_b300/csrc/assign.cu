@@ -22,6 +22,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace smoe {
 namespace {
@@ -77,6 +78,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __shared__ float sh_f[32];
   __shared__ double sh_d[32];
   __shared__ int is_last;
+  grid_dep_wait();
+  grid_dep_launch();
   const int e = blockIdx.x, tid = threadIdx.x;
   const int per = (a.R + kScanThreads - 1) / kScanThreads;
   const int r0 = min(a.R, tid * per), r1 = min(a.R, r0 + per);
@@ -165,6 +168,8 @@ __device__ __forceinline__ void zero_row(float* row, int d, int lane) {
 constexpr int kRowWarps = 8;   // tokens per CTA in the per-token kernels
 
 __global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + warp;
   if (t >= a.T) return;
@@ -189,6 +194,8 @@ __global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a) {
 }
 
 __global__ void __launch_bounds__(kRowWarps * 32) dispatch_kernel(AssignArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + warp;
   if (t >= a.T) return;
@@ -234,6 +241,8 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(AssignArgs a) 
   __shared__ int hist[256];
   __shared__ unsigned long long s_prefix, s_mask;
   __shared__ int s_krem, s_cnt;
+  grid_dep_wait();
+  grid_dep_launch();
   const int e = blockIdx.x, tid = threadIdx.x;
   const int n = a.counts[e];
   if (n == 0) return;
@@ -307,28 +316,26 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(AssignArgs a) 
 
 }  // namespace
 
-cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s) {
-  scan_kernel<<<a.N, kScanThreads, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl) {
+  return launch_k(scan_kernel, dim3(a.N), dim3(kScanThreads), 0, s, pdl, a);
 }
 
-cudaError_t launch_assign(const AssignArgs& a, cudaStream_t s) {
-  assign_kernel<<<(a.T + kRowWarps - 1) / kRowWarps, kRowWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_assign(const AssignArgs& a, cudaStream_t s, bool pdl) {
+  return launch_k(assign_kernel, dim3((a.T + kRowWarps - 1) / kRowWarps), dim3(kRowWarps * 32), 0,
+                  s, pdl, a);
 }
 
-cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s) {
-  dispatch_kernel<<<(a.T + kRowWarps - 1) / kRowWarps, kRowWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s, bool pdl) {
+  return launch_k(dispatch_kernel, dim3((a.T + kRowWarps - 1) / kRowWarps), dim3(kRowWarps * 32),
+                  0, s, pdl, a);
 }
 
-cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s) {
+cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s, bool pdl) {
   const size_t smem = (size_t)kGateSortMax * sizeof(unsigned long long);
   cudaError_t err = cudaFuncSetAttribute(gate_select_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  gate_select_kernel<<<a.N, kSelThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(gate_select_kernel, dim3(a.N), dim3(kSelThreads), smem, s, pdl, a);
 }
 
 }  // namespace smoe

@@ -16,6 +16,7 @@
 //
 // One warp per token, 16-byte vectors along d_model (fp32 in and out).
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace smoe {
 namespace {
@@ -23,6 +24,8 @@ namespace {
 constexpr int kWarps = 8;
 
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + warp;
   if (t >= a.T) return;
@@ -55,9 +58,9 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineArgs a) {
 
 }  // namespace
 
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
-  combine_kernel<<<(a.T + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl) {
+  return launch_k(combine_kernel, dim3((a.T + kWarps - 1) / kWarps), dim3(kWarps * 32), 0, s, pdl,
+                  a);
 }
 
 }  // namespace smoe

@@ -11,6 +11,25 @@
 
 namespace smoe {
 
+// Launch `k` on `s`; with pdl, as a programmatic dependent launch (the
+// kernel may start before the previous kernel of the stream ends and calls
+// grid_dep_wait() before it reads that kernel's results).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t s, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<Args&&>(args)...);
+}
+
 constexpr int kRouterTM = 32;        // tokens per router CTA
 constexpr int kMaxExperts = 1024;
 constexpr int kGateSortMax = 16384;  // keys one gate-priority CTA sorts in shared memory
@@ -43,7 +62,7 @@ int router_tc_n_mma(int N);
 cudaError_t launch_split_wg(const float* W_g, __nv_bfloat16* pieces, int N, int d,
                             cudaStream_t s);
 cudaError_t launch_router_tc(const RouterArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                             int* status, cudaStream_t s);
+                             int* status, cudaStream_t s, bool pdl = false);
 
 // ------------------------------------------------------- scan / tile lists
 struct ScanArgs {
@@ -60,7 +79,7 @@ struct ScanArgs {
   int32_t* split_cnt;     // [n_split_cnt] zeroed for the expert GEMMs' tail split, or null
   int n_split_cnt;
 };
-cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl = false);
 
 // --------------------------------------------- slots, lists, dispatch
 struct AssignArgs {
@@ -84,11 +103,11 @@ struct AssignArgs {
 };
 // Token order: slot, drop and the dispatch copy in one pass.
 // Gate priority: only the per-expert token lists.
-cudaError_t launch_assign(const AssignArgs& a, cudaStream_t s);
+cudaError_t launch_assign(const AssignArgs& a, cudaStream_t s, bool pdl = false);
 // Gate priority: per-expert ranking by (gate desc, token asc); slot and drop.
-cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s);
+cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s, bool pdl = false);
 // Copy kept rows x[t] -> xbuf[e * C + slot[t]] (gate-priority path).
-cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s);
+cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s, bool pdl = false);
 
 // ------------------------------------------------------- expert GEMMs
 // D[e, m, c] = sum_k A[e * M + m, k] * B[e * rows + nt * BN + c, k] for the
@@ -129,9 +148,10 @@ struct GemmArgs {
 };
 // tcgen05 tensor-core path (bf16 operands), TMA-fed.
 cudaError_t launch_gemm_tc(const GemmArgs& g, const CUtensorMap& tmA, const CUtensorMap& tmB0,
-                           const CUtensorMap& tmB1, cudaStream_t s);
+                           const CUtensorMap& tmB1, cudaStream_t s, bool pdl = false);
 // exact-fp32 path (SIMT FFMA) for dtype fp32; A, B are fp32 device pointers.
-cudaError_t launch_gemm_simt(const GemmArgs& g, const float* A, const float* B, cudaStream_t s);
+cudaError_t launch_gemm_simt(const GemmArgs& g, const float* A, const float* B, cudaStream_t s,
+                             bool pdl = false);
 int gemm_tc_max_stages(int BN, int num_b);
 size_t gemm_tc_smem_bytes(int BN, int num_b, int stages);
 
@@ -147,7 +167,7 @@ struct CombineArgs {
   const float* S;           // [T, d] shared-expert output or null
   float* y;                 // [T, d]
 };
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl = false);
 
 // status word of the current device (see switch_moe_sync_status)
 int* device_status_ptr();

@@ -9,6 +9,7 @@
 // a work tile is (expert, 32-token tile, 64-row weight tile);
 //   epi 0: out0 = relu(D) (fp32), epi 1: out0 = D (fp32).
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace smoe {
 namespace {
@@ -19,6 +20,8 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const float* __restrict__
                                                        const float* __restrict__ B, GemmArgs g) {
   __shared__ __align__(16) float As[BK][BM + 4];
   __shared__ __align__(16) float Bs[BK][BNT + 4];
+  grid_dep_wait();
+  grid_dep_launch();
   const int n_entries = g.entries ? *g.n_entries : g.n_entries_dense;
   const int tile = blockIdx.x;
   if (tile >= n_entries * g.m_tiles) return;
@@ -84,10 +87,10 @@ __global__ void __launch_bounds__(NT) gemm_simt_kernel(const float* __restrict__
 
 }  // namespace
 
-cudaError_t launch_gemm_simt(const GemmArgs& g, const float* A, const float* B, cudaStream_t s) {
+cudaError_t launch_gemm_simt(const GemmArgs& g, const float* A, const float* B, cudaStream_t s,
+                             bool pdl) {
   if (g.grid <= 0) return cudaSuccess;
-  gemm_simt_kernel<<<g.grid, NT, 0, s>>>(A, B, g);
-  return cudaGetLastError();
+  return launch_k(gemm_simt_kernel, dim3(g.grid), dim3(NT), 0, s, pdl, A, B, g);
 }
 
 }  // namespace smoe

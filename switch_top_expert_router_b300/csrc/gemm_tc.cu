@@ -34,8 +34,8 @@
 //   warp 0      TMA producer (one lane) into a `stages`-deep shared ring
 //   warp 1      TMEM allocator + MMA issuer (one lane)
 //   warps 2..5  epilogue: TMEM -> registers -> global, 32 TMEM lanes each
-// Two TMEM accumulators let the epilogue of tile i overlap the MMAs of
-// tile i + 1.  Every wait is bounded; on a timeout the CTA records
+// Four TMEM accumulators (two for token tiles over 128) let the epilogue of
+// tile i lag the MMAs of the following tiles.  Every wait is bounded; on a timeout the CTA records
 // SWITCH_MOE_ERR_DEVICE_TIMEOUT, drains its copies and MMAs, frees TMEM and
 // returns.
 #include <cuda_bf16.h>
@@ -50,7 +50,8 @@ constexpr int kThreads = 192;
 constexpr uint32_t kABytes = kTileM * 128;     // 16 KB per stage
 constexpr size_t kSmemLimit = 232448;          // opt-in dynamic shared memory per block
 constexpr size_t kBarrierArea = 512;
-constexpr int kMaxPieces = 8;          // K pieces per split tile
+constexpr int kMaxPieces = 4;          // K pieces per split tile (one round of partial loads)
+constexpr int kMaxAcc = 4;             // TMEM accumulators in flight
 constexpr int kMinPieceKBlocks = 4;    // 256 of K at least per piece
 
 __device__ __forceinline__ void decode_tile(const GemmArgs& g, int tile, int& e, int& nt,
@@ -132,6 +133,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
   atomicExch(status, SWITCH_MOE_ERR_DEVICE_TIMEOUT);
 }
 
+// kEpi: the epilogue (GemmArgs::epi), fixed at compile time so each variant
+// carries only its own store path.
+template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB0,
@@ -143,15 +147,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* tiles = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)g.stages * stage_bytes);
   uint64_t* empty = full + g.stages;
-  uint64_t* tfull = empty + g.stages;   // [2] accumulator ready for the epilogue
-  uint64_t* tempty = tfull + 2;         // [2] accumulator drained by the epilogue
-  uint64_t* drain = tempty + 2;         // [1] MMA drain at teardown
+  uint64_t* tfull = empty + g.stages;   // [kMaxAcc] accumulator ready for the epilogue
+  uint64_t* tempty = tfull + kMaxAcc;   // [kMaxAcc] accumulator drained by the epilogue
+  uint64_t* drain = tempty + kMaxAcc;   // [1] MMA drain at teardown
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // all 512 TMEM columns: four accumulators of 128 columns, or two of 256
   const uint32_t acc_stride = g.BN <= 128 ? 128u : 256u;
-  const uint32_t tmem_cols = 2u * acc_stride;
+  const uint32_t n_acc = 512u / acc_stride;
+  const uint32_t tmem_cols = 512u;
   int* status = g.status;
 
   if (threadIdx.x == 0) {
@@ -159,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxAcc; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 4);
     }
@@ -186,12 +192,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   int full_tiles, pieces;
   split_plan(g, total, full_tiles, pieces);
   const int n_units = full_tiles + (total - full_tiles) * pieces;
+  // The work list comes from two kernels back, complete by now; the B
+  // operand comes from the previous kernel: wait for it.  Thread 0 (the
+  // producer) first starts the weight loads of its first unit.
+  if (threadIdx.x != 0) {
+    grid_dep_wait();
+    grid_dep_launch();
+  }
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
       const uint64_t pol_a = l2_policy_evict_first();   // weights: streamed once
       const uint64_t pol_b = l2_policy_evict_last();    // tokens: reused by every weight tile
+      int pre = 0;   // stages of the first unit whose weights load before the wait
+      if ((int)blockIdx.x < n_units) {
+        Work w0;
+        decode_work(g, blockIdx.x, full_tiles, pieces, w0);
+        pre = min(g.stages, w0.nkb);
+        const int ya = w0.e * g.M + w0.mt * kTileM;
+        for (int kb = 0; kb < pre; ++kb) {
+          mbar_arrive_expect_tx(&full[kb], stage_bytes);
+          tma_load_2d(tiles + (size_t)kb * stage_bytes, &tmA, &full[kb], (w0.kb0 + kb) * kTileK,
+                      ya, pol_a);
+        }
+      }
+      grid_dep_wait();
+      grid_dep_launch();
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
@@ -201,15 +228,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ya = w.e * g.M + w.mt * kTileM;
         const int yb = w.e * g.rows_per_expert + w.nt * g.BN;
         for (int kb = 0; kb < w.nkb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
-                         SWITCH_MOE_ERR_DEVICE_TIMEOUT)) {
-            ok = false;
-            break;
-          }
           uint8_t* st = tiles + (size_t)stage * stage_bytes;
-          mbar_arrive_expect_tx(&full[stage], stage_bytes);
           const int kx = (w.kb0 + kb) * kTileK;
-          tma_load_2d(st, &tmA, &full[stage], kx, ya, pol_a);
+          if (issued >= (uint32_t)pre) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
+                           SWITCH_MOE_ERR_DEVICE_TIMEOUT)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], stage_bytes);
+            tma_load_2d(st, &tmA, &full[stage], kx, ya, pol_a);
+          }
           tma_load_2d(st + kABytes, &tmB0, &full[stage], kx, yb, pol_b);
           if (g.num_b == 2) tma_load_2d(st + kABytes + b_bytes, &tmB1, &full[stage], kx, yb, pol_b);
           ++issued;
@@ -235,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++it) {
         Work w;
         decode_work(g, u, full_tiles, pieces, w);
-        const uint32_t acc = it & 1u, acc_par = (it >> 1) & 1u;
+        const uint32_t acc = it % n_acc, acc_par = (it / n_acc) & 1u;
         if (!mbar_wait(&tempty[acc], acc_par ^ 1u, abort_flag, status,
                        SWITCH_MOE_ERR_DEVICE_TIMEOUT)) {
           ok = false;
@@ -283,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
       Work w;
       decode_work(g, u, full_tiles, pieces, w);
-      const uint32_t acc = it & 1u, acc_par = (it >> 1) & 1u;
+      const uint32_t acc = it % n_acc, acc_par = (it / n_acc) & 1u;
       const int row = w.mt * kTileM + q * 32 + lane;   // weight row = output column
       const bool row_ok = row < g.M;
       const size_t out_row0 = (size_t)w.e * g.rows_per_expert + (size_t)w.nt * g.BN;
@@ -298,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int tk32 = 0;
       float gv32 = 1.f;
-      if (g.epi == 2 && w.unit < 0) tok_gate(0, tk32, gv32);   // overlaps the wait below
+      if (kEpi == 2 && w.unit < 0) tok_gate(0, tk32, gv32);   // overlaps the wait below
       // tcgen05.ld below is warp-collective: leave the loop together or not at all
       const bool ready =
           mbar_wait(&tfull[acc], acc_par, abort_flag, status, SWITCH_MOE_ERR_DEVICE_TIMEOUT);
@@ -306,25 +335,88 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * acc_stride;
 
-      // Stores 16 accumulator columns c0 .. c0 + 15 of this thread's row.
-      auto store_chunk = [&](int c0, const float (&v)[16]) {
-        if (g.epi == 2) {
-          int tk;
-          float gv;
-          tok_gate(c0, tk, gv);   // lanes 16..31 load columns the chunk does not use
-          float* y = static_cast<float*>(g.out0);
+      const size_t tile_elems = (size_t)kTileM * (size_t)g.BN;
+      bool from_tmem = true;   // else: the sum of a split tile's parked partials
+      const float* p0 = nullptr;
+      if (w.unit >= 0) {
+        // one K piece of a split tile: park the partial, [column][128 rows]
+        float* mine = g.part + (size_t)w.unit * tile_elems + q * 32 + lane;
+        for (int c0 = 0; c0 < w.nv; c0 += 16) {
+          float v[16];
+          tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int tj = __shfl_sync(kAll, tk, j);
-            const float gj = __shfl_sync(kAll, gv, j);
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < w.nv) mine[(size_t)(c0 + j) * kTileM] = v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          int32_t* cnt = g.split_cnt + w.sidx * 4 + q;
+          last = atomicAdd(cnt, 1) == w.pieces - 1;
+          if (last) *cnt = 0;   // every piece has arrived: reset for the next launch
+        }
+        if (!__shfl_sync(kAll, last, 0)) continue;
+        __threadfence();
+        from_tmem = false;
+        p0 = g.part + (size_t)w.sidx * w.pieces * tile_elems + q * 32 + lane;
+        if (kEpi == 2) tok_gate(0, tk32, gv32);
+      }
+      // 16 columns c0 .. c0 + 15 of this thread's row into v
+      auto fetch16 = [&](int c0, float (&v)[16]) {
+        if (from_tmem) {
+          tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
+          return;
+        }
+        // every piece's loads in flight at once, then the sum in piece order
+        float t[kMaxPieces][16];
+#pragma unroll
+        for (int i = 0; i < kMaxPieces; ++i) {
+          const float* src = p0 + (size_t)i * tile_elems + (size_t)c0 * kTileM;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            t[i][j] = (i < w.pieces && c0 + j < w.nv) ? __ldcg(src + j * kTileM) : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = t[0][j];
+#pragma unroll
+        for (int i = 1; i < kMaxPieces; ++i) {
+          if (i < w.pieces) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[j] = v[j] + t[i][j];
+          }
+        }
+      };
+
+      if constexpr (kEpi == 2) {
+        // combine: y[token] = g_token * D (+ y[token]), 32 columns per step
+        float* y = static_cast<float*>(g.out0);
+        for (int c0 = 0; c0 < w.nv; c0 += 32) {
+          if (c0 > 0) tok_gate(c0, tk32, gv32);
+          float v[2][16];
+          fetch16(c0, v[0]);
+          fetch16(c0 + 16, v[1]);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int tj = __shfl_sync(kAll, tk32, j);
+            const float gj = __shfl_sync(kAll, gv32, j);
             if (row_ok && c0 + j < w.nv) {
               float* dst = y + (size_t)tj * (size_t)g.ldo + row;
-              const float val = gj * v[j];
+              const float val = gj * v[j >> 4][j & 15];
               *dst = g.y_acc ? *dst + val : val;
             }
           }
-        } else if (row_ok) {
-          if (g.epi == 0) {
+        }
+      } else {
+        for (int c0 = 0; c0 < w.nv; c0 += 16) {
+          float v[16];
+          fetch16(c0, v);
+          if (!row_ok) continue;
+          if constexpr (kEpi == 0) {
+            // relu, then H as an unevaluated bf16 pair hi + lo
             __nv_bfloat16* hi = static_cast<__nv_bfloat16*>(g.out0);
             __nv_bfloat16* lo = static_cast<__nv_bfloat16*>(g.out1);
 #pragma unroll
@@ -345,87 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      };
-
-      if (w.unit < 0 && g.epi == 2) {
-        float* y = static_cast<float*>(g.out0);
-        for (int c0 = 0; c0 < w.nv; c0 += 32) {
-          if (c0 > 0) tok_gate(c0, tk32, gv32);
-          float v[2][16];
-          tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v[0]);
-          tmem_ld_32x32b_x16(taddr + (uint32_t)c0 + 16u, v[1]);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int tj = __shfl_sync(kAll, tk32, j);
-            const float gj = __shfl_sync(kAll, gv32, j);
-            if (row_ok && c0 + j < w.nv) {
-              float* dst = y + (size_t)tj * (size_t)g.ldo + row;
-              const float val = gj * v[j >> 4][j & 15];
-              *dst = g.y_acc ? *dst + val : val;
-            }
-          }
-        }
+      }
+      if (from_tmem) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
-      } else if (w.unit < 0) {
-        for (int c0 = 0; c0 < w.nv; c0 += 16) {
-          float v[16];
-          tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
-          store_chunk(c0, v);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
-      } else {
-        // one K piece of a split tile: park the partial, [column][128 rows]
-        const size_t tile_elems = (size_t)kTileM * (size_t)g.BN;
-        float* mine = g.part + (size_t)w.unit * tile_elems + q * 32 + lane;
-        for (int c0 = 0; c0 < w.nv; c0 += 16) {
-          float v[16];
-          tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < w.nv) mine[(size_t)(c0 + j) * kTileM] = v[j];
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0) {
-          int32_t* cnt = g.split_cnt + w.sidx * 4 + q;
-          last = atomicAdd(cnt, 1) == w.pieces - 1;
-          if (last) *cnt = 0;   // every piece has arrived: reset for the next launch
-        }
-        last = __shfl_sync(kAll, last, 0);
-        if (last) {
-          __threadfence();
-          const float* p0 = g.part + (size_t)w.sidx * w.pieces * tile_elems + q * 32 + lane;
-          for (int c0 = 0; c0 < w.nv; c0 += 16) {
-            // sum in piece order; four pieces' loads in flight at a time
-            float v[16];
-            for (int p4 = 0; p4 < w.pieces; p4 += 4) {
-              float t[4][16];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const float* src = p0 + (size_t)(p4 + i) * tile_elems + (size_t)c0 * kTileM;
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  t[i][j] = (p4 + i < w.pieces && c0 + j < w.nv) ? __ldcg(src + j * kTileM) : 0.f;
-              }
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                if (p4 + i < w.pieces) {
-#pragma unroll
-                  for (int j = 0; j < 16; ++j) v[j] = (p4 + i == 0) ? t[i][j] : v[j] + t[i][j];
-                }
-              }
-            }
-            store_chunk(c0, v);
-          }
-        }
       }
     }
   }
@@ -451,13 +467,12 @@ size_t gemm_tc_smem_bytes(int BN, int num_b, int stages) {
 }
 
 cudaError_t launch_gemm_tc(const GemmArgs& g, const CUtensorMap& tmA, const CUtensorMap& tmB0,
-                           const CUtensorMap& tmB1, cudaStream_t s) {
-  cudaError_t err = cudaFuncSetAttribute(gemm_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)g.smem_bytes);
+                           const CUtensorMap& tmB1, cudaStream_t s, bool pdl) {
+  auto kern = g.epi == 0 ? gemm_tc_kernel<0> : g.epi == 1 ? gemm_tc_kernel<1> : gemm_tc_kernel<2>;
+  cudaError_t err =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_bytes);
   if (err != cudaSuccess) return err;
-  gemm_tc_kernel<<<g.grid, kThreads, g.smem_bytes, s>>>(tmA, tmB0, tmB1, g);
-  return cudaGetLastError();
+  return launch_k(kern, dim3(g.grid), dim3(kThreads), g.smem_bytes, s, pdl, tmA, tmB0, tmB1, g);
 }
 
 }  // namespace smoe

@@ -71,6 +71,21 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return false;
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel of the stream is still running.  grid_dep_wait()
+// blocks the calling thread until that kernel has completed and its memory
+// is visible; grid_dep_launch() lets the next kernel of the stream start.
+// Every kernel of the layer waits before it triggers, so when a kernel
+// starts, all kernels before the previous one have completed.  Both are
+// no-ops for a kernel launched without the attribute.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

@@ -17,6 +17,7 @@
 #include <cuda_bf16.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace smoe {
 namespace {
@@ -152,6 +153,8 @@ __device__ void route_tile(float* lg, int ldl, int T, int N, int t0, int cta,
 template <typename XT>
 __global__ void __launch_bounds__(NTHREADS) router_kernel(RouterArgs a) {
   extern __shared__ float4 smem_f4[];
+  grid_dep_wait();
+  grid_dep_launch();
   float* smem = reinterpret_cast<float*>(smem_f4);
   const int ldl = a.N + 1;
   float* lg = smem;                                  // [TM][N + 1]

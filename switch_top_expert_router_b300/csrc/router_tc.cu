@@ -53,6 +53,7 @@ constexpr size_t kBarrierArea = 256;
 
 __global__ void split_wg_kernel(const float* __restrict__ W_g, __nv_bfloat16* __restrict__ out,
                                 int N, int n_pad, int d) {
+  grid_dep_launch();   // first kernel of the layer: nothing before it is in flight
   const size_t total = (size_t)n_pad * d;
   for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
        idx += (size_t)gridDim.x * blockDim.x) {
@@ -251,21 +252,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x != 0) {   // thread 0, the producer, waits after its first x loads
+    grid_dep_wait();
+    grid_dep_launch();
+  }
 
   if (warp == 0) {
     if (lane == 0) {
       const uint64_t pol_x = l2_policy_evict_first();
       const uint64_t pol_w = l2_policy_evict_last();   // every CTA reads all of W_g
+      // x is the caller's input: its first stages load while the kernel
+      // that splits W_g may still be running
+      const int npre = min(stages, k_blocks);
+      for (int kb = 0; kb < npre; ++kb) {
+        mbar_arrive_expect_tx(&full[kb], stage_bytes);
+        tma_load_2d(tiles + (size_t)kb * stage_bytes, &tmX, &full[kb], kb * kTileK, t0, pol_x);
+      }
+      grid_dep_wait();
+      grid_dep_launch();
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       for (int kb = 0; kb < k_blocks; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
-                       SWITCH_MOE_ERR_DEVICE_TIMEOUT))
-          break;
         uint8_t* st = tiles + (size_t)stage * stage_bytes;
-        mbar_arrive_expect_tx(&full[stage], stage_bytes);
         const int kx = kb * kTileK;
-        tma_load_2d(st, &tmX, &full[stage], kx, t0, pol_x);
+        if (kb >= npre) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
+                         SWITCH_MOE_ERR_DEVICE_TIMEOUT))
+            break;
+          mbar_arrive_expect_tx(&full[stage], stage_bytes);
+          tma_load_2d(st, &tmX, &full[stage], kx, t0, pol_x);
+        }
         for (int pc = 0; pc < 3; ++pc)
           tma_load_2d(st + kXBytes + pc * w_bytes, &tmW, &full[stage], kx, pc * n_mma, pol_w);
         ++issued;
@@ -484,7 +500,7 @@ cudaError_t launch_split_wg(const float* W_g, __nv_bfloat16* pieces, int N, int 
 }
 
 cudaError_t launch_router_tc(const RouterArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                             int* status, cudaStream_t s) {
+                             int* status, cudaStream_t s, bool pdl) {
   const int n_mma = router_tc_n_mma(a.N);
   const int stages = router_tc_stages(a.N, a.d);
   const size_t smem = router_tc_smem_bytes(a.N, a.d);
@@ -494,9 +510,8 @@ cudaError_t launch_router_tc(const RouterArgs& a, const CUtensorMap& tmX, const 
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int grid = (a.T + 127) / 128;
-  kern<<<grid, kThreads, smem, s>>>(tmX, tmW, a, n_mma, (a.d + kTileK - 1) / kTileK, stages,
-                                    status);
-  return cudaGetLastError();
+  return launch_k(kern, dim3(grid), dim3(kThreads), smem, s, pdl, tmX, tmW, a, n_mma,
+                  (a.d + kTileK - 1) / kTileK, stages, status);
 }
 
 }  // namespace smoe
