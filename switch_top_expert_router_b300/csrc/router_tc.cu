@@ -21,8 +21,8 @@
 // at 5120 when all of K accumulates in TMEM, against 2.7e-7 / 1.8e-6 for
 // sequential FFMA).  So each 64-wide K block (4 k-steps x 3 pieces = 12
 // MMAs) accumulates into a fresh TMEM accumulator, and the epilogue warps
-// add that block sum into an fp32 running sum kept in TMEM -- exact fp32
-// additions, one per block.  Two block accumulators alternate so the MMAs of
+// add that block sum into an fp32 running sum -- in registers for up to 128
+// experts, else in TMEM -- with exact fp32 additions, one per block.  Two block accumulators alternate so the MMAs of
 // block k+1 overlap the promotion of block k (one when 3 x N columns do not
 // fit in TMEM).
 //
@@ -31,10 +31,10 @@
 //   warp 0     TMA: x tile [128 x 64] + the three W_g pieces [n x 64]
 //   warp 1     TMEM allocator + MMA issuer (3 MMAs per 16-wide k step)
 //   warps 2-5  promotion of every K block, then the epilogue: one thread
-//              per token, its N logits read from TMEM
-//              in increasing expert order -- the same operation sequence as
-//              the FFMA router's epilogue, so both route identical logits
-//              identically, bit for bit.
+//              per token runs its N logits (staged in shared memory, or read
+//              from TMEM) in increasing expert order -- the same operation
+//              sequence as the FFMA router's epilogue, so both route
+//              identical logits identically, bit for bit.
 // Outputs per group of 32 tokens (one epilogue warp), the layout the scan
 // expects: expert histogram, each token's rank among earlier same-expert
 // tokens of the group, and the group's sum of probabilities per expert.
@@ -71,80 +71,74 @@ __global__ void split_wg_kernel(const float* __restrict__ W_g, __nv_bfloat16* __
 
 constexpr int kRegExperts = 128;   // experts whose running sums fit in registers
 
-// Outputs of one token group (32 tokens = one epilogue warp) from the
-// finished logits: expert id, gate, per-expert probability sums of the
-// group and its histogram plus in-group ranks.  l[] holds the token's
-// logits on entry (bias added); it is overwritten with exp(l - max).
-__device__ __forceinline__ void route_token_regs(const RouterArgs& a, float (&l)[kRegExperts],
-                                                 uint8_t* tiles, int* cnt_s, int q, int lane,
-                                                 int t0, int t, bool valid) {
+// Row stride (floats) of the finished logits staged in shared memory for the
+// routing step: odd, so a warp reading one column of 32 rows, or 32
+// consecutive columns of one row, touches 32 different banks.
+constexpr int kEpiLd = kRegExperts + 1;
+constexpr size_t kEpiBytes = (size_t)128 * kEpiLd * 4 + 128 * 4;   // logits + 1 / sums
+
+// Routing of one epilogue warp's 32 tokens from their logits, staged in
+// shared memory (row r = token t0 + r): expert id, gate, the group's
+// per-expert probability sums and its histogram plus in-group ranks.  Each
+// thread runs its token's row in increasing expert order, the same
+// operation sequence as the FFMA router, so both route identical logits
+// bit for bit.  Compact loops: this code runs once per launch, so its size,
+// not its trip count, is what costs.
+__device__ __noinline__ void route_group_smem(const RouterArgs& a, float* lg, float* invs,
+                                              int* cnt_s, int q, int lane, int t0) {
   const int N = a.N, T = a.T;
+  const int r = q * 32 + lane;
+  const int t = t0 + r;
+  const bool valid = t < T;
+  float* row = lg + (size_t)r * kEpiLd;
   if (a.logits_out) {   // debug entry point: the logits only
-    if (valid) {
-#pragma unroll
-      for (int i = 0; i < kRegExperts; ++i)
-        if (i < N) a.logits_out[(size_t)t * N + i] = l[i];
-    }
+    if (valid)
+      for (int i = 0; i < N; ++i) a.logits_out[(size_t)t * N + i] = row[i];
     return;
   }
-  // max and first argmax, increasing expert order
   float m = -INFINITY;
   int mi = 0;
-#pragma unroll
-  for (int i = 0; i < kRegExperts; ++i) {
-    if (i < N && l[i] > m) {
-      m = l[i];
+  for (int i = 0; i < N; ++i) {
+    const float v = row[i];
+    if (v > m) {
+      m = v;
       mi = i;
     }
   }
-  // sum of exp(l - m), sequential in expert order
   float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < kRegExperts; ++i) {
-    if (i < N) {
-      l[i] = expf(l[i] - m);
-      s += l[i];
-    }
+  for (int i = 0; i < N; ++i) {
+    const float e = expf(row[i] - m);
+    row[i] = e;
+    s += e;
   }
   const float inv = 1.0f / s;
-  const int g = blockIdx.x * 4 + q;                // 32-token group
-  const bool group_ok = t0 + q * 32 < T;
+  invs[r] = inv;
   if (valid) {
     a.expert_id[t] = mi;
     a.gate[t] = inv;   // exp(0) / s: the probability of the argmax
   }
-  // Group sums of the probabilities, 32 experts at a time, transposed
-  // through this warp's [32][33] slice of the (now idle) pipeline buffers;
-  // tokens past T contribute zeros.
-  float* pw = reinterpret_cast<float*>(tiles) + (size_t)q * 32 * 33;
-#pragma unroll
-  for (int c0 = 0; c0 < kRegExperts; c0 += 32) {
-    if (c0 < N) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (c0 + j < N) pw[lane * 33 + j] = valid ? l[c0 + j] * inv : 0.f;
-      __syncwarp();
-      if (group_ok && c0 + lane < N) {
-        float acc = 0.f;
-        for (int r = 0; r < 32; ++r) acc += pw[r * 33 + lane];
-        a.P_part[(size_t)g * N + c0 + lane] = acc;
-      }
-      __syncwarp();
-    }
+  __syncwarp();
+  const int nvalid = min(32, T - (t0 + q * 32));
+  if (nvalid <= 0) return;
+  const int g = blockIdx.x * 4 + q;   // 32-token group
+  // group sums of p = exp(l - m) / s per expert, tokens in order
+  const float* rows = lg + (size_t)q * 32 * kEpiLd;
+  for (int c = lane; c < N; c += 32) {
+    float acc = 0.f;
+    for (int rr = 0; rr < nvalid; ++rr) acc += rows[(size_t)rr * kEpiLd + c] * invs[q * 32 + rr];
+    a.P_part[(size_t)g * N + c] = acc;
   }
-  if (group_ok) {
-    // histogram and rank among earlier same-expert tokens of the group
-    const int e = valid ? mi : -1 - lane;
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    int* hs = cnt_s + q * N;
-    if (valid) {
-      const unsigned lt = (1u << lane) - 1u;
-      a.local_rank[t] = __popc(peers & lt);
-      if ((peers & lt) == 0) hs[e] = __popc(peers);
-    }
-    __syncwarp();
-    for (int i = lane; i < N; i += 32) a.hist[(size_t)g * N + i] = hs[i];
+  // histogram and rank among earlier same-expert tokens of the group
+  const int e = valid ? mi : -1 - lane;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  int* hs = cnt_s + q * N;
+  if (valid) {
+    const unsigned lt = (1u << lane) - 1u;
+    a.local_rank[t] = __popc(peers & lt);
+    if ((peers & lt) == 0) hs[e] = __popc(peers);
   }
+  __syncwarp();
+  for (int i = lane; i < N; i += 32) a.hist[(size_t)g * N + i] = hs[i];
 }
 
 // Epilogue warps for N <= kRegExperts: promote every K block's TMEM sum
@@ -188,10 +182,14 @@ __device__ __forceinline__ void router_epilogue_regs(
     __syncwarp();
     if (lane == 0) mbar_arrive(&tempty[b]);
   }
+  // stage the finished logits (bias added) in the idle pipeline buffers
+  float* lg = reinterpret_cast<float*>(tiles);
+  float* row = lg + (size_t)(q * 32 + lane) * kEpiLd;
 #pragma unroll
   for (int i = 0; i < kRegExperts; ++i)
-    if (i < a.N) run[i] = run[i] + bias_s[i];
-  route_token_regs(a, run, tiles, cnt_s, q, lane, t0, t, valid);
+    if (i < a.N) row[i] = run[i] + bias_s[i];
+  __syncwarp();
+  route_group_smem(a, lg, lg + (size_t)128 * kEpiLd, cnt_s, q, lane, t0);
 }
 
 // kRegs (N <= kRegExperts): each epilogue thread keeps its token's running
@@ -205,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t w_bytes = (uint32_t)n_mma * 128u;
   const uint32_t stage_bytes = kXBytes + 3u * w_bytes;
   uint8_t* tiles = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)stages * stage_bytes);
+  const size_t tile_area = max((size_t)stages * stage_bytes, kEpiBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + tile_area);
   uint64_t* empty = full + stages;
   uint64_t* tfull = empty + stages;   // [2] block accumulator ready
   uint64_t* tempty = tfull + 2;       // [2] block accumulator promoted
@@ -485,8 +484,9 @@ int router_tc_stages(int N, int d) {
 
 size_t router_tc_smem_bytes(int N, int d) {
   const size_t stage = kXBytes + 3u * (size_t)router_tc_n_mma(N) * 128u;
-  return (size_t)router_tc_stages(N, d) * stage + 1024 + kBarrierArea +
-         (size_t)kMaxExpertsTc * 4 * 5;
+  size_t area = (size_t)router_tc_stages(N, d) * stage;
+  if (area < kEpiBytes) area = kEpiBytes;   // the routing step reuses the stage buffers
+  return area + 1024 + kBarrierArea + (size_t)kMaxExpertsTc * 4 * 5;
 }
 
 cudaError_t launch_split_wg(const float* W_g, __nv_bfloat16* pieces, int N, int d,
