@@ -47,8 +47,8 @@ from workloads import CONFIGS, expert_weights, make_inputs, zipf_bias  # noqa: E
 # (mean of GEMM 1 and GEMM 2).  Valid only for the kernel source it was
 # taken on; any other source reports null.
 NCU_TRAFFIC = {
-    "base": {"gemm_tc_sha256": "4fecb544c6a2be62d1972239cfc7e93e6096ad52640a4615b826b0eeda3a5ae3",
-             "bytes_per_launch": (672.7e6 + 751.7e6) / 2},
+    "base": {"gemm_tc_sha256": "40c9a708b396dd6e90041abf1ecc1f4b4f8871a6ce0a16967d60e0e9001d5036",
+             "bytes_per_launch": ((625.726 + 47.451) + (737.521 + 14.766)) * 1e6 / 2},
 }
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
@@ -241,7 +241,7 @@ def workload_config(w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
     ap.add_argument("--config", default="base", choices=sorted(CONFIGS))
