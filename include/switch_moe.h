@@ -222,9 +222,11 @@ const char* switch_moe_strerror(int code);
  * stream it runs on.  events == NULL switches recording off.  Returns
  * SWITCH_MOE_ERR_INVALID_ARG when n != SWITCH_MOE_NUM_PHASE_EVENTS.
  *   0 start              1 after the router        2 after the scan (L_aux)
- *   3 after slots + dispatch                       4 after expert GEMM 1
- *   5 after the shared-expert GEMMs (== 4 without one)
- *   6 after expert GEMM 2                          7 after combine */
+ *   3 after slots + dispatch
+ *   4 after the shared-expert GEMMs (== 3 without one)
+ *   5 after the routed experts' GEMM 1 (== 4 when one launch runs both layers)
+ *   6 after the routed experts' GEMM 2
+ *   7 after combine (== 6 when GEMM 2's epilogue combines) */
 #define SWITCH_MOE_NUM_PHASE_EVENTS 8
 int switch_moe_set_phase_events(void* const* events, int n);
 

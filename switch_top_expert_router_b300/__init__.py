@@ -51,7 +51,7 @@ EXPORTED = (
     "switch_moe_route_from_logits_noalloc",
 )
 NUM_PHASE_EVENTS = 8
-PHASES = ("router", "scan_aux", "slots_dispatch", "expert_gemm1", "shared_gemms",
+PHASES = ("router", "scan_aux", "slots_dispatch", "shared_gemms", "expert_gemm1",
           "expert_gemm2", "combine")
 
 

@@ -100,6 +100,7 @@ struct Plan {
   int max_entries;   // N * ceil(C / BN)
   int ksplit;        // K splits of the second routed GEMM
   bool fused;        // combine in the second routed GEMM's epilogue (tensor path, ksplit 1)
+  bool ffn;          // fused and BN <= 128: both routed GEMMs in one launch (ffn_tc_kernel)
   int part_units;    // tail-split partial tiles of the tensor-core GEMMs
   // workspace offsets
   bool tc_router;    // bf16 x and N <= kMaxExpertsTc: tensor-core router
@@ -194,10 +195,13 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
     } else {
       q.o_O = take((size_t)q.ksplit * NC * q.d * 4);
     }
+    q.ffn = q.fused && q.BN <= 128;
     if (q.bf16) {
       q.part_units = kPlanSMs;
       q.o_part = take((size_t)q.part_units * kTileM * q.BN * 4);
-      q.o_splitcnt = take((size_t)4 * q.part_units * 4);
+      // tail-split counters, then the fused FFN's per-work-item counters and
+      // its unit counter; the scan zeroes them every forward
+      q.o_splitcnt = take((size_t)(4 * q.part_units + q.max_entries + 1) * 4);
     }
     if (q.shared) {
       if (q.bf16) {
@@ -281,7 +285,7 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   sa.entries = at<int2>(ws, q.o_entries); sa.BN = q.BN; sa.ctrl = ctrl;
   if (dispatch && q.part_units) {
     sa.split_cnt = at<int32_t>(ws, q.o_splitcnt);
-    sa.n_split_cnt = 4 * q.part_units;
+    sa.n_split_cnt = 4 * q.part_units + q.max_entries + 1;
   }
   if (launch_scan(sa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   mark(2, s);
@@ -375,6 +379,48 @@ int run_gemm(const Plan& q, const DeviceInfo* dev, bool dense, int layer, const 
   return SWITCH_MOE_OK;
 }
 
+// Both routed GEMMs in one persistent launch (ffn_tc_kernel).
+int run_ffn(const Plan& q, const DeviceInfo* dev, const void* W1, const void* W2, float* y,
+            const int32_t* counts, const float* gate, void* ws, cudaStream_t s) {
+  FfnArgs a{};
+  a.C = q.C; a.BN = q.BN; a.d = (int)q.d; a.F = (int)q.F;
+  a.m1 = (int)cdiv(q.F, kTileM); a.kb1 = (int)cdiv(q.d, kTileK);
+  a.m2 = (int)cdiv(q.d, kTileM); a.kb2 = (int)cdiv(q.F, kTileK);
+  a.entries = at<int2>(ws, q.o_entries);
+  a.n_entries = at<int32_t>(ws, q.o_ctrl) + 1;
+  a.counts = counts; a.cap = q.C;
+  const int64_t units_max = (int64_t)q.max_entries * (a.m1 + a.m2);
+  a.grid = (int)(units_max < dev->sms ? units_max : dev->sms);
+  if (a.grid < 1) return SWITCH_MOE_OK;
+  // a block's GEMM 1 tiles cover about 1.25 waves of the grid, so a block's
+  // GEMM 2 tiles start after its GEMM 1 tiles have finished
+  int64_t eb = cdiv((int64_t)a.grid * 5, 4 * (int64_t)a.m1);
+  const int64_t eb_min = cdiv(q.max_entries, kFfnMaxBlocks);
+  if (eb < eb_min) eb = eb_min;
+  if (eb < 1) eb = 1;
+  a.eb = (int)eb;
+  a.dep = at<int32_t>(ws, q.o_splitcnt) + 4 * q.part_units;
+  a.sched = a.dep + q.max_entries;
+  a.H0 = at<__nv_bfloat16>(ws, q.o_H0); a.H1 = at<__nv_bfloat16>(ws, q.o_H1);
+  a.y = y; a.tok_of_slot = at<int32_t>(ws, q.o_tok); a.gate = gate;
+  a.gate_multiply = q.gm; a.y_acc = q.shared;
+  a.part = at<float>(ws, q.o_part); a.part_units = q.part_units;
+  a.split_cnt = at<int32_t>(ws, q.o_splitcnt);
+  a.stages = ffn_tc_stages(q.BN);
+  a.smem_bytes = ffn_tc_smem_bytes(q.BN, a.stages);
+  a.status = dev->status;
+  const uint64_t rows = (uint64_t)q.N * q.C;
+  CUtensorMap tw1, tx, tw2, th0, th1;
+  if (!make_map(&tw1, W1, (uint64_t)q.N * q.F, (uint64_t)q.d, kTileM) ||
+      !make_map(&tx, at<void>(ws, q.o_xbuf), rows, (uint64_t)q.d, (uint32_t)q.BN) ||
+      !make_map(&tw2, W2, (uint64_t)q.N * q.d, (uint64_t)q.F, kTileM) ||
+      !make_map(&th0, a.H0, rows, (uint64_t)q.F, (uint32_t)q.BN) ||
+      !make_map(&th1, a.H1, rows, (uint64_t)q.F, (uint32_t)q.BN))
+    return SWITCH_MOE_ERR_CUDA;
+  if (launch_ffn_tc(a, tw1, tx, tw2, th0, th1, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  return SWITCH_MOE_OK;
+}
+
 int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const float* W_g,
                    const float* b_g, const void* W1, const void* W2, const void* W1s,
                    const void* W2s, float* y, int32_t* expert_id, float* gate, int32_t* slot,
@@ -385,9 +431,8 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
   void* xbuf = at<void>(ws, q.o_xbuf);
   void* H0 = at<void>(ws, q.o_H0);
   void* H1 = q.bf16 ? at<void>(ws, q.o_H1) : nullptr;
-  if ((rc = run_gemm(q, dev, false, 1, W1, xbuf, nullptr, H0, H1, counts, gate, ws, s)))
-    return rc;
-  mark(4, s);
+  // shared expert first: with the fused combine it writes y, which the
+  // routed experts' second GEMM then accumulates into
   float* Os = nullptr;
   if (q.shared) {
     void* Hs0 = at<void>(ws, q.o_Hs0);
@@ -398,6 +443,16 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
     if ((rc = run_gemm(q, dev, true, 2, W2s, Hs0, Hs1, Os, nullptr, nullptr, gate, ws, s)))
       return rc;
   }
+  mark(4, s);
+  if (q.ffn) {
+    mark(5, s);   // one launch runs both layers
+    if ((rc = run_ffn(q, dev, W1, W2, y, counts, gate, ws, s))) return rc;
+    mark(6, s);
+    mark(7, s);
+    return SWITCH_MOE_OK;
+  }
+  if ((rc = run_gemm(q, dev, false, 1, W1, xbuf, nullptr, H0, H1, counts, gate, ws, s)))
+    return rc;
   mark(5, s);
   if (q.fused) {
     // combine runs in the epilogue of the second routed GEMM

@@ -155,6 +155,42 @@ cudaError_t launch_gemm_simt(const GemmArgs& g, const float* A, const float* B, 
 int gemm_tc_max_stages(int BN, int num_b);
 size_t gemm_tc_smem_bytes(int BN, int num_b, int stages);
 
+// ------------------------------------------------------- fused expert FFN
+// GEMM 1 (+ ReLU, H hi + lo) and GEMM 2 (+ combine into y) of the routed
+// experts in one persistent launch (tensor path, token tile <= 128).
+constexpr int kFfnMaxBlocks = 256;   // blocks of work items in the schedule
+struct FfnArgs {
+  int C, BN;                  // slots per expert, token tile
+  int d, F;                   // d_model, d_ff
+  int m1, kb1;                // GEMM 1: 128-row tiles over F, 64-wide K blocks over d
+  int m2, kb2;                // GEMM 2: 128-row tiles over d, 64-wide K blocks over F
+  const int2* entries;        // work items (expert, token tile)
+  const int32_t* n_entries;   // device count of work items
+  const int32_t* counts;      // kept_e = min(counts[e], cap)
+  int cap;
+  int eb;                     // work items per schedule block
+  int32_t* dep;               // [work items] GEMM 1 slices stored; zero on entry
+  int32_t* sched;             // [1] next unit to claim; zero on entry
+  __nv_bfloat16* H0;          // [N * C, F] hi
+  __nv_bfloat16* H1;          // [N * C, F] lo
+  float* y;                   // [T, d]
+  const int32_t* tok_of_slot; // [N * C]
+  const float* gate;          // [T]
+  int gate_multiply, y_acc;
+  float* part;                // tail split partials [part_units][128 * BN], or null
+  int part_units;
+  int32_t* split_cnt;         // [4 * part_units]
+  int stages;
+  int* status;
+  int grid;
+  size_t smem_bytes;
+};
+int ffn_tc_stages(int BN);
+size_t ffn_tc_smem_bytes(int BN, int stages);
+cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap& tmW1, const CUtensorMap& tmX,
+                          const CUtensorMap& tmW2, const CUtensorMap& tmH0,
+                          const CUtensorMap& tmH1, cudaStream_t s, bool pdl);
+
 // ------------------------------------------------------- combine
 struct CombineArgs {
   int T, d, C, ksplit;
