@@ -43,26 +43,28 @@ import torch  # noqa: E402
 from workloads import CONFIGS, expert_weights, make_inputs, zipf_bias  # noqa: E402
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of
-# gemm_tc_kernel, from the ncu capture summarised in profiles/gemm_tc_base.md
-# (mean of GEMM 1 and GEMM 2).  Valid only for the kernel source it was
-# taken on; any other source reports null.
+# the dominant kernel, from the ncu captures summarised in profiles/: the
+# one-launch expert FFN (ffn_tc_kernel) where the workload uses it, else the
+# mean of the two gemm_tc_kernel launches.  Valid only for the kernel source
+# it was taken on (sha256 of the .cu file); any other source reports null.
 NCU_TRAFFIC = {
-    "base": {"gemm_tc_sha256": "40c9a708b396dd6e90041abf1ecc1f4b4f8871a6ce0a16967d60e0e9001d5036",
-             "bytes_per_launch": ((625.726 + 47.451) + (737.521 + 14.766)) * 1e6 / 2},
+    "base": {"source": "ffn_tc.cu",
+             "sha256": "7f6275b361c33e0ae7f077934eab58c3723bdfa7ecf7c2aca7b5b54708f54d44",
+             "bytes_per_launch": (1267.072 + 87.484) * 1e6},
 }
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 CPU_SAMPLE_EXPERTS = 16
 
 
-def gemm_traffic(config: str):
+def kernel_traffic(config: str):
     rec = NCU_TRAFFIC.get(config)
     if not rec:
         return None
     import hashlib
-    src = os.path.join(ROOT, "switch_top_expert_router_b300", "csrc", "gemm_tc.cu")
+    src = os.path.join(ROOT, "switch_top_expert_router_b300", "csrc", rec["source"])
     with open(src, "rb") as f:
-        if hashlib.sha256(f.read()).hexdigest() != rec["gemm_tc_sha256"]:
+        if hashlib.sha256(f.read()).hexdigest() != rec["sha256"]:
             return None
     return rec["bytes_per_launch"]
 
@@ -337,8 +339,17 @@ def main():
     g1_bytes = active * wbytes_expert + T_kept * d * eb + T_kept * F * eb
     g2_bytes = active * wbytes_expert + T_kept * F * eb + T_kept * d * 4
     gemm_ms = phase_ms["expert_gemm1"] + phase_ms["expert_gemm2"]
+    tc_router = w.dtype == "bf16" and w.N <= 256
+    fused = w.dtype == "bf16" and gemm2_ksplit(w, C) == 1
+    ffn_one = fused and -(-C // 16) * 16 <= 128   # both routed GEMMs in one launch
+    # algorithmic bytes of the dominant kernel per launch: the active experts'
+    # weights, the dispatched tokens in and the expert outputs out -- and,
+    # when GEMM 1 and GEMM 2 are separate launches, H out of one and into the
+    # other (the mean of the two launches)
+    ffn_bytes = (2 * active * wbytes_expert + T_kept * d * eb + T_kept * d * 4 if ffn_one
+                 else (g1_bytes + g2_bytes) / 2)
     hbm, bf16_peak, peak_kind = peaks()
-    achieved = (g1_bytes + g2_bytes) / (gemm_ms / 1e3) / 1e9
+    achieved = ffn_bytes * (1 if ffn_one else 2) / (gemm_ms / 1e3) / 1e9
     layer_bytes = (w.T * d * eb + w.T * d * 4 + w.N * d * 4 + w.T * 13 + w.N * 4
                    + 2 * active * wbytes_expert + (2 * wbytes_expert if w.has_shared else 0))
     layer_flops = 4.0 * T_kept * d * F + (4.0 * w.T * d * F if w.has_shared else 0.0)
@@ -346,10 +357,8 @@ def main():
     # kernels per forward: [split W_g +] router, scan, slots/dispatch [+ gate
     # ranking + dispatch], GEMM 1 [+ shared GEMMs], GEMM 2 [+ combine when the
     # second GEMM's epilogue cannot do it: fp32 layers, K-split GEMM 2]
-    tc_router = w.dtype == "bf16" and w.N <= 256
-    fused = w.dtype == "bf16" and gemm2_ksplit(w, C) == 1
-    launches = ((2 if tc_router else 1) + 2 + (2 if w.priority_mode else 0) + 2
-                + (2 if w.has_shared else 0) + (0 if fused else 1))
+    launches = ((2 if tc_router else 1) + 2 + (2 if w.priority_mode else 0)
+                + (1 if ffn_one else 2) + (2 if w.has_shared else 0) + (0 if fused else 1))
 
     # ---- end to end through the host-buffer entry point
     e2e = None
@@ -402,11 +411,13 @@ def main():
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": workload_config(w),
             "e2e": e2e,
-            "roofline": {"kernel": "gemm_tc_kernel (expert GEMM 1 + 2)", "bound": "hbm",
+            "roofline": {"kernel": ("ffn_tc_kernel (expert GEMM 1 + 2, one launch)" if ffn_one
+                                    else "gemm_tc_kernel (expert GEMM 1 + 2)"),
+                         "bound": "hbm",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_kind": peak_kind,
-                         "traffic": gemm_traffic(args.config),
-                         "algorithmic_bytes_per_launch": (g1_bytes + g2_bytes) / 2},
+                         "traffic": kernel_traffic(args.config) if ffn_one else None,
+                         "algorithmic_bytes_per_launch": ffn_bytes},
             "layer_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": 1e3 * ms / args.steps,
                                "frac": t_roof / (ms / args.steps / 1e3),
                                "bytes": layer_bytes, "flops": layer_flops,
