@@ -10,6 +10,8 @@
 // overflow section plus the token-path flowchart (nodes D -> F): once every
 // score is known, an over-full expert keeps its highest-weight tokens.
 //
+// Dispatch: each kept row is copied x[t] -> buffer[e, slot] by two TMA bulk
+//   copies through shared memory (the load starts before the slot is known).
 // Token order:   slot(t) = #{t' < t : e(t') = e(t)}; kept iff slot < C.
 //   The router already produced, per CTA of 32 tokens, an expert histogram
 //   and each token's rank inside its CTA; scan_kernel turns the histograms
@@ -167,12 +169,59 @@ __device__ __forceinline__ void zero_row(float* row, int d, int lane) {
 
 constexpr int kRowWarps = 8;   // tokens per CTA in the per-token kernels
 
+// Rows up to this size are staged through shared memory by TMA bulk copies;
+// longer rows use the vector copy.
+constexpr uint32_t kStageRowMax = 16384;
+
+// Bounded wait on a bulk copy's mbarrier (one thread); false on timeout.
+__device__ __forceinline__ bool row_wait(uint64_t* bar, int* status) {
+  const unsigned long long t0 = globaltimer_ns();
+  for (unsigned it = 0; it < kWaitMaxIters; ++it) {
+    if (mbar_try_wait(bar, 0u)) return true;
+    if ((it & 31u) == 31u && globaltimer_ns() - t0 > kWaitTimeoutNs) break;
+  }
+  atomicExch(status, SWITCH_MOE_ERR_DEVICE_TIMEOUT);
+  return false;
+}
+
+// Dispatch of token t's row into the expert buffer (row `dst_row`, or no copy
+// when dst_row < 0), staged through this warp's slot of shared memory:
+// the TMA load was started by stage_row_begin before the destination was
+// known; lane 0 waits for it and issues the TMA store.
+__device__ __forceinline__ void stage_row_begin(const AssignArgs& a, uint8_t* buf, uint64_t* bar,
+                                                int t, uint32_t rb, int lane) {
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    fence_barrier_init();
+    mbar_arrive_expect_tx(bar, rb);
+    bulk_load(buf, static_cast<const char*>(a.x) + (size_t)t * rb, rb, bar);
+  }
+}
+__device__ __forceinline__ void stage_row_end(const AssignArgs& a, uint8_t* buf, uint64_t* bar,
+                                              int e, int dst_row, uint32_t rb, int lane) {
+  if (lane == 0) {
+    // the load must land before the CTA may exit, copied or not
+    if (row_wait(bar, a.status) && dst_row >= 0) {
+      fence_proxy_async_smem();
+      bulk_store(static_cast<char*>(a.xbuf) + ((size_t)e * a.C + dst_row) * rb, buf, rb);
+      bulk_commit();
+      bulk_wait_read();
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a) {
+  extern __shared__ __align__(128) uint8_t rowbuf[];   // [kRowWarps][rb] when staged
+  __shared__ __align__(8) uint64_t rowbar[kRowWarps];
   grid_dep_wait();
   grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + warp;
   if (t >= a.T) return;
+  const uint32_t rb = (uint32_t)a.d * (uint32_t)a.elem_bytes;
+  const bool staged = a.mode == SWITCH_MOE_TOKEN_ORDER && a.xbuf && rb <= kStageRowMax;
+  uint8_t* buf = rowbuf + (size_t)warp * rb;
+  if (staged) stage_row_begin(a, buf, &rowbar[warp], t, rb, lane);   // x row is known already
   const int e = a.expert_id[t];
   const int s = a.bases[(size_t)(t / kRouterTM) * a.N + e] + a.local_rank[t];
   if (a.mode == SWITCH_MOE_TOKEN_ORDER) {
@@ -180,12 +229,13 @@ __global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a) {
     if (lane == 0) {
       a.slot[t] = kept ? s : -1;
       a.drop[t] = kept ? 0 : 1;
+      if (kept && a.xbuf && a.tok_of_slot) a.tok_of_slot[(size_t)e * a.C + s] = t;
     }
-    if (kept && a.xbuf) {   // no buffer when only routing (route_from_logits)
-      const size_t rb = (size_t)a.d * a.elem_bytes;
+    if (staged) {
+      stage_row_end(a, buf, &rowbar[warp], e, kept ? s : -1, rb, lane);
+    } else if (kept && a.xbuf) {   // no buffer when only routing (route_from_logits)
       copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
                static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
-      if (a.tok_of_slot && lane == 0) a.tok_of_slot[(size_t)e * a.C + s] = t;
     }
     if (!kept && a.y) zero_row(a.y + (size_t)t * a.d, a.d, lane);
   } else if (lane == 0) {
@@ -194,21 +244,27 @@ __global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a) {
 }
 
 __global__ void __launch_bounds__(kRowWarps * 32) dispatch_kernel(AssignArgs a) {
+  extern __shared__ __align__(128) uint8_t rowbuf[];
+  __shared__ __align__(8) uint64_t rowbar[kRowWarps];
   grid_dep_wait();
   grid_dep_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + warp;
   if (t >= a.T) return;
+  const uint32_t rb = (uint32_t)a.d * (uint32_t)a.elem_bytes;
+  const bool staged = rb <= kStageRowMax;
+  uint8_t* buf = rowbuf + (size_t)warp * rb;
+  if (staged) stage_row_begin(a, buf, &rowbar[warp], t, rb, lane);
   const int s = a.slot[t];
-  if (s < 0) {
-    if (a.y) zero_row(a.y + (size_t)t * a.d, a.d, lane);
-    return;
-  }
   const int e = a.expert_id[t];
-  const size_t rb = (size_t)a.d * a.elem_bytes;
-  copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
-           static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
-  if (a.tok_of_slot && lane == 0) a.tok_of_slot[(size_t)e * a.C + s] = t;
+  if (s >= 0 && a.tok_of_slot && lane == 0) a.tok_of_slot[(size_t)e * a.C + s] = t;
+  if (staged) {
+    stage_row_end(a, buf, &rowbar[warp], e, s, rb, lane);
+  } else if (s >= 0) {
+    copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
+             static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
+  }
+  if (s < 0 && a.y) zero_row(a.y + (size_t)t * a.d, a.d, lane);
 }
 
 constexpr int kSelThreads = 1024;
@@ -320,14 +376,31 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl) {
   return launch_k(scan_kernel, dim3(a.N), dim3(kScanThreads), 0, s, pdl, a);
 }
 
+// Dynamic shared memory of the row-staging kernels: one row per warp when
+// the rows are staged through TMA.
+static size_t row_stage_smem(const AssignArgs& a, bool dispatch) {
+  const size_t rb = (size_t)a.d * a.elem_bytes;
+  const bool staged = (dispatch || (a.mode == SWITCH_MOE_TOKEN_ORDER && a.xbuf)) &&
+                      rb <= kStageRowMax;
+  return staged ? (size_t)kRowWarps * rb : 0;
+}
+
 cudaError_t launch_assign(const AssignArgs& a, cudaStream_t s, bool pdl) {
-  return launch_k(assign_kernel, dim3((a.T + kRowWarps - 1) / kRowWarps), dim3(kRowWarps * 32), 0,
-                  s, pdl, a);
+  const size_t smem = row_stage_smem(a, false);
+  cudaError_t err =
+      cudaFuncSetAttribute(assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  return launch_k(assign_kernel, dim3((a.T + kRowWarps - 1) / kRowWarps), dim3(kRowWarps * 32),
+                  smem, s, pdl, a);
 }
 
 cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s, bool pdl) {
+  const size_t smem = row_stage_smem(a, true);
+  cudaError_t err = cudaFuncSetAttribute(dispatch_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
   return launch_k(dispatch_kernel, dim3((a.T + kRowWarps - 1) / kRowWarps), dim3(kRowWarps * 32),
-                  0, s, pdl, a);
+                  smem, s, pdl, a);
 }
 
 cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s, bool pdl) {
