@@ -283,6 +283,9 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   sa.C = q.C; sa.counts = counts; sa.P_sum = at<float>(ws, q.o_Psum);
   sa.expert_start = at<int32_t>(ws, q.o_start); sa.aux_loss = aux;
   sa.entries = at<int2>(ws, q.o_entries); sa.BN = q.BN; sa.ctrl = ctrl;
+  // token order: the assign kernel finishes the pass over experts (work
+  // list, L_aux) in an extra CTA while its other CTAs place the tokens
+  sa.defer_finish = q.mode == SWITCH_MOE_TOKEN_ORDER;
   if (dispatch && q.part_units) {
     sa.split_cnt = at<int32_t>(ws, q.o_splitcnt);
     sa.n_split_cnt = 4 * q.part_units + q.max_entries + 1;
@@ -299,7 +302,8 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   aa.tok_of_slot = (dispatch && q.fused) ? at<int32_t>(ws, q.o_tok) : nullptr;
   aa.y = (dispatch && q.fused && !q.shared) ? y : nullptr;
   aa.status = status;
-  if (launch_assign(aa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  if (launch_assign(aa, sa.defer_finish ? &sa : nullptr, s, true) != cudaSuccess)
+    return SWITCH_MOE_ERR_CUDA;
   if (q.mode == SWITCH_MOE_GATE_PRIORITY) {
     if (launch_gate_select(aa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
     if (dispatch && launch_dispatch(aa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
@@ -401,6 +405,8 @@ int run_ffn(const Plan& q, const DeviceInfo* dev, const void* W1, const void* W2
   a.eb = (int)eb;
   a.dep = at<int32_t>(ws, q.o_splitcnt) + 4 * q.part_units;
   a.sched = a.dep + q.max_entries;
+  a.W1 = W1;
+  a.n_experts = (int)q.N;
   a.H0 = at<__nv_bfloat16>(ws, q.o_H0); a.H1 = at<__nv_bfloat16>(ws, q.o_H1);
   a.y = y; a.tok_of_slot = at<int32_t>(ws, q.o_tok); a.gate = gate;
   a.gate_multiply = q.gm; a.y_acc = q.shared;

@@ -75,42 +75,13 @@ __device__ F block_sum(F v, F* sh /*[32]*/) {
   return r;   // valid in thread 0
 }
 
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
-  __shared__ int sh_i[33];
-  __shared__ float sh_f[32];
-  __shared__ double sh_d[32];
-  __shared__ int is_last;
-  grid_dep_wait();
-  grid_dep_launch();
-  const int e = blockIdx.x, tid = threadIdx.x;
-  const int per = (a.R + kScanThreads - 1) / kScanThreads;
-  const int r0 = min(a.R, tid * per), r1 = min(a.R, r0 + per);
-  int cnt = 0;
-  float ps = 0.f;
-  for (int r = r0; r < r1; ++r) {
-    cnt += a.hist[(size_t)r * a.N + e];
-    ps += a.P_part[(size_t)r * a.N + e];
-  }
-  int total;
-  int run = block_exclusive_scan(cnt, &total, sh_i);
-  for (int r = r0; r < r1; ++r) {
-    const size_t i = (size_t)r * a.N + e;
-    const int v = a.hist[i];
-    a.hist[i] = run;
-    run += v;
-  }
-  const float psum = block_sum<float>(ps, sh_f);
-  if (tid == 0) {
-    a.counts[e] = total;
-    a.P_sum[e] = psum;
-    __threadfence();
-    is_last = (atomicAdd(&a.ctrl[0], 1) == a.N - 1);
-  }
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-
-  // ---- last CTA: prefix of counts, L_aux, GEMM work items -------------
+// After every expert's count and probability sum are stored: exclusive
+// prefix of the counts, the GEMM work items (expert, token tile) in expert
+// order, L_aux, and zeroed counters for the expert GEMMs.  Run by one CTA
+// of kScanThreads threads: the last scan CTA to finish, or (token order)
+// an extra CTA of the slot-assignment kernel, off the scan's critical path.
+__device__ void finish_experts(const ScanArgs& a, int* sh_i, double* sh_d) {
+  const int tid = threadIdx.x;
   // Each thread owns a contiguous run of up to 4 experts.
   const int per_e = (a.N + kScanThreads - 1) / kScanThreads;   // <= 4 for N <= 1024
   const int e0 = min(a.N, tid * per_e), e1 = min(a.N, e0 + per_e);
@@ -144,6 +115,47 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
     a.aux_loss[0] = (float)((double)a.N * aux / (T * T));  // N * sum (c_i / T)(P_i / T)
     a.ctrl[0] = 0;
   }
+}
+
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
+  __shared__ int sh_i[33];
+  __shared__ float sh_f[32];
+  __shared__ double sh_d[32];
+  __shared__ int is_last;
+  grid_dep_wait();
+  grid_dep_launch();
+  const int e = blockIdx.x, tid = threadIdx.x;
+  const int per = (a.R + kScanThreads - 1) / kScanThreads;
+  const int r0 = min(a.R, tid * per), r1 = min(a.R, r0 + per);
+  int cnt = 0;
+  float ps = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    cnt += a.hist[(size_t)r * a.N + e];
+    ps += a.P_part[(size_t)r * a.N + e];
+  }
+  int total;
+  int run = block_exclusive_scan(cnt, &total, sh_i);
+  for (int r = r0; r < r1; ++r) {
+    const size_t i = (size_t)r * a.N + e;
+    const int v = a.hist[i];
+    a.hist[i] = run;
+    run += v;
+  }
+  const float psum = block_sum<float>(ps, sh_f);
+  if (tid == 0) {
+    a.counts[e] = total;
+    a.P_sum[e] = psum;
+  }
+  if (a.defer_finish) return;   // the slot-assignment kernel runs finish_experts
+  if (tid == 0) {
+    __threadfence();
+    is_last = (atomicAdd(&a.ctrl[0], 1) == a.N - 1);
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+
+  finish_experts(a, sh_i, sh_d);
 }
 
 // Copy one row of `bytes` (a multiple of 16) with the lanes of a warp.
@@ -210,11 +222,17 @@ __device__ __forceinline__ void stage_row_end(const AssignArgs& a, uint8_t* buf,
   }
 }
 
-__global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a) {
+__global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a, ScanArgs sa) {
   extern __shared__ __align__(128) uint8_t rowbuf[];   // [kRowWarps][rb] when staged
   __shared__ __align__(8) uint64_t rowbar[kRowWarps];
   grid_dep_wait();
   grid_dep_launch();
+  if (sa.defer_finish && blockIdx.x == gridDim.x - 1) {   // the extra CTA
+    __shared__ int sh_i[33];
+    __shared__ double sh_d[32];
+    finish_experts(sa, sh_i, sh_d);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kRowWarps + warp;
   if (t >= a.T) return;
@@ -385,13 +403,15 @@ static size_t row_stage_smem(const AssignArgs& a, bool dispatch) {
   return staged ? (size_t)kRowWarps * rb : 0;
 }
 
-cudaError_t launch_assign(const AssignArgs& a, cudaStream_t s, bool pdl) {
+cudaError_t launch_assign(const AssignArgs& a, const ScanArgs* finish, cudaStream_t s, bool pdl) {
   const size_t smem = row_stage_smem(a, false);
   cudaError_t err =
       cudaFuncSetAttribute(assign_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_k(assign_kernel, dim3((a.T + kRowWarps - 1) / kRowWarps), dim3(kRowWarps * 32),
-                  smem, s, pdl, a);
+  ScanArgs sa{};
+  if (finish) sa = *finish;
+  const int grid = (a.T + kRowWarps - 1) / kRowWarps + (sa.defer_finish ? 1 : 0);
+  return launch_k(assign_kernel, dim3(grid), dim3(kRowWarps * 32), smem, s, pdl, a, sa);
 }
 
 cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s, bool pdl) {

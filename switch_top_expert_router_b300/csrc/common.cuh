@@ -78,6 +78,9 @@ struct ScanArgs {
   int32_t* ctrl;          // ctrl[0] done counter, ctrl[1] number of entries
   int32_t* split_cnt;     // [n_split_cnt] zeroed for the expert GEMMs' tail split, or null
   int n_split_cnt;
+  // 1: the scan stores counts / probability sums only; finish_experts (prefix,
+  // work list, L_aux) runs in an extra CTA of the slot-assignment kernel
+  int defer_finish;
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl = false);
 
@@ -103,7 +106,10 @@ struct AssignArgs {
 };
 // Token order: slot, drop and the dispatch copy in one pass.
 // Gate priority: only the per-expert token lists.
-cudaError_t launch_assign(const AssignArgs& a, cudaStream_t s, bool pdl = false);
+// finish (token order, or null): the scan's arguments when it ran with
+// defer_finish; one extra CTA then completes the pass over experts.
+cudaError_t launch_assign(const AssignArgs& a, const ScanArgs* finish, cudaStream_t s,
+                          bool pdl = false);
 // Gate priority: per-expert ranking by (gate desc, token asc); slot and drop.
 cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s, bool pdl = false);
 // Copy kept rows x[t] -> xbuf[e * C + slot[t]] (gate-priority path).
@@ -171,6 +177,8 @@ struct FfnArgs {
   int eb;                     // work items per schedule block
   int32_t* dep;               // [work items] GEMM 1 slices stored; zero on entry
   int32_t* sched;             // [1] next unit to claim; zero on entry
+  const void* W1;             // [N, F, d] (L2 prefetch hint before the dependency wait)
+  int n_experts;
   __nv_bfloat16* H0;          // [N * C, F] hi
   __nv_bfloat16* H1;          // [N * C, F] lo
   float* y;                   // [T, d]

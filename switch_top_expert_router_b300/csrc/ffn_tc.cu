@@ -175,7 +175,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *abort_flag = 0;
     fence_barrier_init();
-    // the schedule (the work list comes from two kernels back: complete)
+  }
+  if (threadIdx.x == 32) {
+    prefetch_tensormap(&tmW1);
+    prefetch_tensormap(&tmX);
+    prefetch_tensormap(&tmW2);
+    prefetch_tensormap(&tmH0);
+    prefetch_tensormap(&tmH1);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (threadIdx.x == 0) {
+    // While the previous kernel finishes: pull into L2 the W1 tile this CTA
+    // most likely claims first (unit blockIdx.x, taking work item j to be
+    // expert j, as when every expert has one token tile).  Only a hint: a
+    // wrong guess costs bandwidth, never a result.
+    const int j = blockIdx.x / a.m1, mt = blockIdx.x - (blockIdx.x / a.m1) * a.m1;
+    const size_t row = (size_t)j * a.F + (size_t)mt * kTileM;
+    if (row + kTileM <= (size_t)a.n_experts * a.F) {
+      const char* base = static_cast<const char*>(a.W1) + row * (size_t)a.d * 2;
+      const uint32_t bytes = kTileM * (uint32_t)a.d * 2u;
+      for (uint32_t off = 0; off < bytes; off += 32768u)
+        l2_prefetch_bulk(base + off, min(32768u, bytes - off));
+    }
+  }
+  grid_dep_wait();   // the work list, its counters and the expert buffer
+  grid_dep_launch();
+  if (threadIdx.x == 0) {
+    // the schedule over the work list of the previous kernel
     const int ne = *a.n_entries;
     const int B = (ne + a.eb - 1) / a.eb;
     int n = 0, pos = 0;
@@ -196,21 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sg.start[n] = pos;
     sg.n = n;
   }
-  if (threadIdx.x == 32) {
-    prefetch_tensormap(&tmW1);
-    prefetch_tensormap(&tmX);
-    prefetch_tensormap(&tmW2);
-    prefetch_tensormap(&tmH0);
-    prefetch_tensormap(&tmH1);
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, tmem_cols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
 
   const int total = sg.n > 0 ? sg.start[sg.n] : 0;
   // tail split: only the list's last GEMM 2 tiles are cut
@@ -228,10 +247,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   const int n_units = full_tiles + (total - full_tiles) * pieces;
-  if (threadIdx.x != 0) {
-    grid_dep_wait();
-    grid_dep_launch();
-  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -254,23 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       int p = n_units;
-      bool ok = claim(p);   // the counter was zeroed two kernels back
-      int pre = 0;          // first unit's weight stages issued before the wait
-      if (ok && p < n_units) {
-        Unit u0;
-        int c0 = 0;
-        decode_unit(a, sg, c0, p, full_tiles, pieces, u0);
-        if (u0.kind == 1) {
-          pre = min(a.stages, u0.nkb);
-          for (int kb = 0; kb < pre; ++kb) {
-            mbar_arrive_expect_tx(&full[kb], tx1);
-            tma_load_2d(tiles + (size_t)kb * stage_bytes, &tmW1, &full[kb],
-                        (u0.kb0 + kb) * kTileK, u0.e * a.F + u0.mt * kTileM, pol_a);
-          }
-        }
-      }
-      grid_dep_wait();
-      grid_dep_launch();
+      bool ok = claim(p);
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       while (ok && p < n_units) {
@@ -289,15 +288,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < u.nkb; ++kb) {
           uint8_t* st = tiles + (size_t)stage * stage_bytes;
           const int kx = (u.kb0 + kb) * kTileK;
-          if (issued >= (uint32_t)pre) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
-                           SWITCH_MOE_ERR_DEVICE_TIMEOUT)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&full[stage], g1 ? tx1 : tx2);
-            tma_load_2d(st, mA, &full[stage], kx, ya, pol_a);
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
+                         SWITCH_MOE_ERR_DEVICE_TIMEOUT)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(&full[stage], g1 ? tx1 : tx2);
+          tma_load_2d(st, mA, &full[stage], kx, ya, pol_a);
           if (g1) {
             tma_load_2d(st + kABytes, &tmX, &full[stage], kx, yb, pol_b);
           } else {

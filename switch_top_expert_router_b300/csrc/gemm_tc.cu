@@ -186,39 +186,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the work list and the B operand come from the kernel before this one
+  grid_dep_wait();
+  grid_dep_launch();
 
   const int n_entries = g.entries ? *g.n_entries : g.n_entries_dense;
   const int total = n_entries * g.m_tiles * g.ksplit;
   int full_tiles, pieces;
   split_plan(g, total, full_tiles, pieces);
   const int n_units = full_tiles + (total - full_tiles) * pieces;
-  // The work list comes from two kernels back, complete by now; the B
-  // operand comes from the previous kernel: wait for it.  Thread 0 (the
-  // producer) first starts the weight loads of its first unit.
-  if (threadIdx.x != 0) {
-    grid_dep_wait();
-    grid_dep_launch();
-  }
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------- producer
       const uint64_t pol_a = l2_policy_evict_first();   // weights: streamed once
       const uint64_t pol_b = l2_policy_evict_last();    // tokens: reused by every weight tile
-      int pre = 0;   // stages of the first unit whose weights load before the wait
-      if ((int)blockIdx.x < n_units) {
-        Work w0;
-        decode_work(g, blockIdx.x, full_tiles, pieces, w0);
-        pre = min(g.stages, w0.nkb);
-        const int ya = w0.e * g.M + w0.mt * kTileM;
-        for (int kb = 0; kb < pre; ++kb) {
-          mbar_arrive_expect_tx(&full[kb], stage_bytes);
-          tma_load_2d(tiles + (size_t)kb * stage_bytes, &tmA, &full[kb], (w0.kb0 + kb) * kTileK,
-                      ya, pol_a);
-        }
-      }
-      grid_dep_wait();
-      grid_dep_launch();
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
@@ -230,15 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < w.nkb; ++kb) {
           uint8_t* st = tiles + (size_t)stage * stage_bytes;
           const int kx = (w.kb0 + kb) * kTileK;
-          if (issued >= (uint32_t)pre) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
-                           SWITCH_MOE_ERR_DEVICE_TIMEOUT)) {
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&full[stage], stage_bytes);
-            tma_load_2d(st, &tmA, &full[stage], kx, ya, pol_a);
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
+                         SWITCH_MOE_ERR_DEVICE_TIMEOUT)) {
+            ok = false;
+            break;
           }
+          mbar_arrive_expect_tx(&full[stage], stage_bytes);
+          tma_load_2d(st, &tmA, &full[stage], kx, ya, pol_a);
           tma_load_2d(st + kABytes, &tmB0, &full[stage], kx, yb, pol_b);
           if (g.num_b == 2) tma_load_2d(st + kABytes + b_bytes, &tmB1, &full[stage], kx, yb, pol_b);
           ++issued;

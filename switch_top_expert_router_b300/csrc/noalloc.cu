@@ -132,7 +132,7 @@ extern "C" int switch_moe_route_from_logits_noalloc(const switch_moe_params* p,
   aa.counts = expert_counts; aa.expert_start = sa.expert_start;
   aa.sorted_list = at<int32_t>(ws, kOffList); aa.slot = slot; aa.drop = drop_mask;
   aa.x = nullptr; aa.xbuf = nullptr; aa.status = status;
-  if (launch_assign(aa, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  if (launch_assign(aa, nullptr, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   if (p->priority_mode == SWITCH_MOE_GATE_PRIORITY && launch_gate_select(aa, s) != cudaSuccess)
     return SWITCH_MOE_ERR_CUDA;
   return SWITCH_MOE_OK;

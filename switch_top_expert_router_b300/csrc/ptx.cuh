@@ -127,6 +127,11 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Asynchronous prefetch of `bytes` (a multiple of 16) at a 16-byte aligned
+// global address into L2; nothing waits for it.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* gptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
 // 2-D tiled bulk tensor load global -> shared, completing on `bar`.
 // x is the inner (contiguous) coordinate in elements; it must be a multiple
 // of 16 bytes' worth of elements (callers pass multiples of the 128-byte box).
