@@ -58,7 +58,7 @@ __all__ = [
     "TOKEN_ORDER", "GATE_PRIORITY",
     "capacity", "router_logits", "softmax", "top1", "route", "route_from_logits",
     "assign_slots", "expert_ffn", "aux_loss", "combine_token", "forward",
-    "forward_rows",
+    "forward_rows", "candidates", "assign_slots_expanded",
 ]
 
 TOKEN_ORDER = 0
@@ -191,6 +191,51 @@ def assign_slots(expert_id, gate, N: int, C: int, priority_mode: int = TOKEN_ORD
 
 
 # --------------------------------------------------------------------------
+# Expanded Drop ([CAP] inference section, on Capacity-Aware Inference: the
+# tokens an over-full expert drops consider further experts of their
+# candidate set, so the spare capacity of under-used experts is used).
+# The page gives the idea in one sentence; the reading taken here:
+#   * a token's candidate set is its experts in descending logit order
+#     (lowest index first on ties), the first k of them;
+#   * pass 1 is the top-1 assignment with capacity C in token order;
+#   * in pass r = 2..k every token still unplaced, in token order, takes
+#     the next free slot of its r-th candidate if that expert has one;
+#   * a token placed in pass r is processed by that expert, with that
+#     expert's probability as its gate; expert_counts (f_i) and L_aux keep
+#     the router's top-1 choices.
+# k = 1 is the plain top-1 assignment.
+# --------------------------------------------------------------------------
+def candidates(logits, k: int) -> np.ndarray:
+    """int64 [T, k]: each token's experts by descending logit, lowest index
+    first among equal logits."""
+    l = _f64(logits)
+    order = np.argsort(-l, axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
+
+
+def assign_slots_expanded(cands, N: int, C: int):
+    """Returns (expert int64[T] processing each token -- its first
+    candidate when dropped --, slot int64[T] with -1 for dropped,
+    drop uint8[T], used int64[N] = filled slots per expert)."""
+    cands = np.asarray(cands, dtype=np.int64)
+    T, k = cands.shape
+    used = np.zeros(N, dtype=np.int64)
+    expert = cands[:, 0].copy()
+    slot = np.full(T, -1, dtype=np.int64)
+    for r in range(k):                        # pass r + 1
+        for t in range(T):                    # token order
+            if slot[t] >= 0:
+                continue
+            e = cands[t, r]
+            if used[e] < C:
+                slot[t] = used[e]
+                used[e] += 1
+                expert[t] = e
+    drop = (slot < 0).astype(np.uint8)
+    return expert, slot, drop, used
+
+
+# --------------------------------------------------------------------------
 # Step a6/a7: the expert, a two-layer bias-free FFN ([TOP1] key-parameter
 # section: about 2 * d_model * d_ff weights per expert).  ReLU between.
 #   W1_e: [d_ff, d_model], W2_e: [d_model, d_ff] (out-features first).
@@ -233,30 +278,38 @@ def combine_token(o_row: Optional[np.ndarray], gate: float, dropped: bool,
 
 def forward(x, W_g, W1, W2, capacity_factor: float, priority_mode: int = TOKEN_ORDER,
             gate_multiply: int = 1, b_g=None, W1s=None, W2s=None,
-            expert_getter: Optional[Callable[[int], tuple]] = None):
+            expert_getter: Optional[Callable[[int], tuple]] = None, expand: int = 1):
     """The whole layer on one batch.
 
     W1 / W2 are [N, F, d] / [N, d, F]; alternatively ``expert_getter(e)``
     returns (W1_e, W2_e) so that large layers need not be held whole.
-    Returns a dict with y (fp64 [T, d]), routing outputs and aux_loss."""
+    expand > 1: Expanded Drop over the first `expand` candidates (token
+    order only).  Returns a dict with y (fp64 [T, d]), routing outputs
+    (expert_id / gate of the processing expert) and aux_loss."""
     r = route(x, W_g, b_g)
     T, N = r["probs"].shape
     C = capacity(T, N, capacity_factor)
     slot, drop, counts = assign_slots(r["expert_id"], r["gate"], N, C, priority_mode)
+    expert_id, gate = r["expert_id"], r["gate"]
+    if expand > 1:
+        if priority_mode != TOKEN_ORDER:
+            raise ValueError("Expanded Drop is defined for token-order priority")
+        expert_id, slot, drop, _ = assign_slots_expanded(candidates(r["logits"], expand), N, C)
+        gate = r["probs"][np.arange(T), expert_id]
     d = x.shape[1]
     y = np.zeros((T, d), dtype=np.float64)
     o = np.zeros((T, d), dtype=np.float64)
     for i in range(N):
-        rows = np.nonzero((r["expert_id"] == i) & (slot >= 0))[0]
+        rows = np.nonzero((expert_id == i) & (slot >= 0))[0]
         if rows.size == 0:
             continue
         W1_e, W2_e = expert_getter(i) if expert_getter else (W1[i], W2[i])
         o[rows] = expert_ffn(_rows(x, rows), W1_e, W2_e)
     S = expert_ffn(x, W1s, W2s) if W1s is not None else None
     for t in range(T):
-        y[t] = combine_token(o[t], r["gate"][t], bool(drop[t]), bool(gate_multiply), d,
+        y[t] = combine_token(o[t], gate[t], bool(drop[t]), bool(gate_multiply), d,
                              None if S is None else S[t])
-    return {"y": y, "expert_id": r["expert_id"], "gate": r["gate"], "slot": slot,
+    return {"y": y, "expert_id": expert_id, "gate": gate, "slot": slot,
             "drop": drop, "counts": counts, "aux_loss": aux_loss(r["probs"], counts),
             "logits": r["logits"], "probs": r["probs"], "capacity": C}
 

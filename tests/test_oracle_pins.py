@@ -406,3 +406,112 @@ def test_forward_rows_matches_forward():
     part = O.forward_rows(rows, x, full["expert_id"], full["gate"], full["slot"], 1,
                           lambda e: (W1[e], W2[e]), W1s, W2s)
     np.testing.assert_allclose(part, full["y"][rows], rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------ Expanded Drop
+def _golden_expanded():
+    rows, cands, N, C = [], None, 0, 0
+    for line in open(os.path.join(GOLDEN, "expanded_drop.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        if line.startswith("cands"):
+            f = line.split()
+            N, C = int(f[1].split("=")[1]), int(f[2].split("=")[1])
+            cands = np.array([[int(v) for v in c.split(",")] for c in f[3:]])
+            continue
+        k, e, s, u = (part.split() for part in line.split("|"))
+        rows.append((cands, N, C, int(k[0]), [int(v) for v in e], [int(v) for v in s],
+                     [int(v) for v in u]))
+    return rows
+
+
+@pytest.mark.parametrize("case", _golden_expanded(),
+                         ids=lambda c: f"N{c[1]}C{c[2]}k{c[3]}")
+def test_expanded_drop_golden(case):
+    cands, N, C, k, want_e, want_s, want_u = case
+    e, s, drop, used = O.assign_slots_expanded(cands[:, :k], N, C)
+    assert e.tolist() == want_e and s.tolist() == want_s and used.tolist() == want_u
+    assert drop.tolist() == [int(v < 0) for v in want_s]
+
+
+def test_candidates_order_and_ties():
+    rng = np.random.default_rng(3)
+    l = rng.integers(-2, 3, size=(200, 6)).astype(np.float64)   # many exact ties
+    c = O.candidates(l, 6)
+    for t in range(l.shape[0]):
+        want = sorted(range(6), key=lambda i: (-l[t, i], i))    # logit desc, index asc
+        assert c[t].tolist() == want
+    # the first candidate is the top-1 expert of the forward
+    e, _ = O.top1(l, O.softmax(l))
+    assert np.array_equal(c[:, 0], e)
+
+
+def test_expanded_drop_k1_is_top1_token_order():
+    rng = np.random.default_rng(4)
+    for T, N, C in [(300, 5, 40), (64, 8, 3), (50, 2, 30)]:
+        l = rng.normal(size=(T, N))
+        c = O.candidates(l, 1)
+        e, s, d, used = O.assign_slots_expanded(c, N, C)
+        s0, d0, counts = O.assign_slots(c[:, 0], np.ones(T), N, C, O.TOKEN_ORDER)
+        assert np.array_equal(s, s0) and np.array_equal(d, d0)
+        assert np.array_equal(used, np.minimum(counts, C)) and np.array_equal(e, c[:, 0])
+
+
+def test_expanded_drop_invariants():
+    rng = np.random.default_rng(5)
+    for T, N, C in [(400, 6, 50), (128, 4, 20), (1000, 16, 40), (37, 3, 1)]:
+        l = rng.normal(size=(T, N)) + np.linspace(0, 2, N)   # skewed towards high experts
+        prev_drops = None
+        for k in range(1, N + 1):
+            c = O.candidates(l, k)
+            e, s, d, used = O.assign_slots_expanded(c, N, C)
+            assert np.all(used <= C)
+            for i in range(N):   # each expert's slots are 0 .. used - 1, once each
+                assert sorted(s[(e == i) & (s >= 0)].tolist()) == list(range(used[i]))
+            kept = s >= 0
+            # a kept token runs on one of its first k candidates; a dropped
+            # token found every one of them full
+            assert all(e[t] in c[t].tolist() for t in np.nonzero(kept)[0])
+            assert all(used[c[t]].min() == C for t in np.nonzero(~kept)[0])
+            drops = int(d.sum())
+            assert prev_drops is None or drops <= prev_drops   # more candidates, fewer drops
+            prev_drops = drops
+        if N * C >= T:   # with every candidate allowed, nothing is dropped
+            assert prev_drops == 0
+
+
+def test_expanded_drop_no_drops_when_capacity_suffices():
+    rng = np.random.default_rng(6)
+    T, N = 200, 4
+    C = O.capacity(T, N, float(N))   # cf >= N: C >= T
+    l = rng.normal(size=(T, N))
+    c = O.candidates(l, 3)
+    e, s, d, _ = O.assign_slots_expanded(c, N, C)
+    assert d.sum() == 0 and np.array_equal(e, c[:, 0])   # all placed in pass 1
+
+
+def test_forward_expanded_reroutes_with_candidate_gate():
+    rng = np.random.default_rng(7)
+    T, d, F, N = 96, 16, 24, 4
+    x = torch.tensor(rng.normal(size=(T, d)))
+    W_g = torch.tensor(rng.normal(size=(N, d)) * 0.5)
+    W_g[0] += 0.8   # expert 0 over-full
+    W1 = torch.tensor(rng.normal(size=(N, F, d)) / np.sqrt(d))
+    W2 = torch.tensor(rng.normal(size=(N, d, F)) / np.sqrt(F))
+    base = O.forward(x, W_g, W1, W2, 1.0)
+    ex = O.forward(x, W_g, W1, W2, 1.0, expand=2)
+    assert ex["drop"].sum() < base["drop"].sum()
+    assert ex["aux_loss"] == base["aux_loss"] and np.array_equal(ex["counts"], base["counts"])
+    moved = np.nonzero((base["drop"] == 1) & (ex["drop"] == 0))[0]
+    assert moved.size > 0
+    c2 = O.candidates(base["logits"], 2)
+    for t in moved:
+        e = int(c2[t, 1])
+        assert ex["expert_id"][t] == e
+        assert ex["gate"][t] == base["probs"][t, e]
+        h = torch.relu(x[t] @ W1[e].T)                         # library routines, float64
+        assert np.allclose(ex["y"][t], (base["probs"][t, e] * (h @ W2[e].T)).numpy(),
+                           rtol=1e-12, atol=1e-12)
+    same = np.nonzero(base["drop"] == 0)[0]                  # pass-1 tokens are untouched
+    assert np.array_equal(ex["y"][same], base["y"][same])
