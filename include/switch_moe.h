@@ -98,6 +98,15 @@ typedef struct switch_moe_params {
   int32_t gate_multiply;    /* 1: y = gate * E(x) ([SWITCH] Eq. 2); 0: y = E(x) ([TOP1] step 3) */
   int32_t dtype;            /* enum switch_moe_dtype */
   int32_t has_shared;       /* 1: add an always-on shared expert W1s/W2s ([CMP]) */
+  /* Expanded Drop ([CAP] inference section): 0 or 1 = off (plain top-1);
+   * k in 2..4 = each token's candidate set is its first k experts by logit
+   * (lowest index first on ties); tokens the top-1 pass drops take, in token
+   * order, the next free slot of their 2nd, then 3rd, ... candidate.  A
+   * re-routed token runs on that expert with that expert's probability as
+   * its gate; expert_id / gate / slot report the expert that runs it.
+   * expert_counts and aux_loss keep the router's top-1 choices.  Token-order
+   * priority only (SWITCH_MOE_ERR_UNSUPPORTED otherwise); k <= N. */
+  int32_t expand;
 } switch_moe_params;
 
 /* Expert capacity C = ceil(cf * T / N), evaluated in double as (cf*T)/N.

@@ -62,6 +62,7 @@ class Params(ctypes.Structure):
         ("N", ctypes.c_int64), ("capacity_factor", ctypes.c_double),
         ("priority_mode", ctypes.c_int32), ("gate_multiply", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("has_shared", ctypes.c_int32),
+        ("expand", ctypes.c_int32),
     ]
 
 
@@ -180,9 +181,10 @@ def switch_moe_capacity(T: int, N: int, capacity_factor: float) -> int:
 
 
 def make_params(T, d_model, d_ff, N, capacity_factor, priority_mode=TOKEN_ORDER,
-                gate_multiply=1, dtype=BF16, has_shared=0) -> Params:
+                gate_multiply=1, dtype=BF16, has_shared=0, expand=1) -> Params:
     return Params(int(T), int(d_model), int(d_ff), int(N), float(capacity_factor),
-                  int(priority_mode), int(gate_multiply), int(dtype), int(has_shared))
+                  int(priority_mode), int(gate_multiply), int(dtype), int(has_shared),
+                  int(expand))
 
 
 def switch_moe_workspace_bytes(p: Params) -> int:
@@ -250,15 +252,16 @@ def switch_moe_forward(x: torch.Tensor, W_g: torch.Tensor, W1: torch.Tensor, W2:
                        gate_multiply: int = 1, b_g: Optional[torch.Tensor] = None,
                        W1s: Optional[torch.Tensor] = None, W2s: Optional[torch.Tensor] = None,
                        ws: Optional[torch.Tensor] = None, out: Optional[ForwardOut] = None,
-                       stream=None) -> ForwardOut:
-    """The whole layer; see switch_moe_forward in include/switch_moe.h."""
+                       stream=None, expand: int = 1) -> ForwardOut:
+    """The whole layer; see switch_moe_forward in include/switch_moe.h
+    (expand: Expanded Drop candidates, 1 = off)."""
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor (use switch_moe_forward_hostio for host data)")
     dev = x.device
     _contig(x, "x", None, dev)
     T, d, F, N = _layer_args(x, W_g, W1, W2, b_g, W1s, W2s, dev)
     p = make_params(T, d, F, N, capacity_factor, priority_mode, gate_multiply, _dtype_code(x),
-                    int(W1s is not None))
+                    int(W1s is not None), expand)
     need = switch_moe_workspace_bytes(p)
     if ws is None:
         ws = workspace(need, dev)
@@ -287,7 +290,8 @@ def switch_moe_forward_hostio(x_host: torch.Tensor, W_g: torch.Tensor, W1: torch
                               W1s: Optional[torch.Tensor] = None,
                               W2s: Optional[torch.Tensor] = None,
                               ws: Optional[torch.Tensor] = None,
-                              out: Optional[ForwardOut] = None, stream=None) -> ForwardOut:
+                              out: Optional[ForwardOut] = None, stream=None,
+                              expand: int = 1) -> ForwardOut:
     """Host input and output tensors (pin them for asynchronous copies);
     device weights.  Outputs are valid after the stream is synchronised."""
     if x_host.is_cuda:
@@ -296,7 +300,7 @@ def switch_moe_forward_hostio(x_host: torch.Tensor, W_g: torch.Tensor, W1: torch
     _contig(x_host, "x_host")
     T, d, F, N = _layer_args(x_host, W_g, W1, W2, b_g, W1s, W2s, dev)
     p = make_params(T, d, F, N, capacity_factor, priority_mode, gate_multiply,
-                    _dtype_code(x_host), int(W1s is not None))
+                    _dtype_code(x_host), int(W1s is not None), expand)
     need = switch_moe_hostio_workspace_bytes(p)
     if ws is None:
         ws = workspace(need, dev)
@@ -322,12 +326,12 @@ def switch_moe_forward_hostio(x_host: torch.Tensor, W_g: torch.Tensor, W1: torch
 def switch_moe_route_from_logits(logits: torch.Tensor, capacity_factor: float,
                                  priority_mode: int = TOKEN_ORDER,
                                  ws: Optional[torch.Tensor] = None,
-                                 stream=None) -> RouteOut:
-    """Routing on given fp32 logits [T, N]."""
+                                 stream=None, expand: int = 1) -> RouteOut:
+    """Routing on given fp32 logits [T, N] (expand: Expanded Drop candidates)."""
     dev = logits.device
     _contig(logits, "logits", torch.float32)
     T, N = logits.shape
-    p = make_params(T, 8, 8, N, capacity_factor, priority_mode, 1, F32, 0)
+    p = make_params(T, 8, 8, N, capacity_factor, priority_mode, 1, F32, 0, expand)
     need = switch_moe_workspace_bytes(p)
     if ws is None:
         ws = workspace(need, dev)

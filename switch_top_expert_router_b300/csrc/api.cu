@@ -95,6 +95,7 @@ struct Plan {
   int C, R;
   bool bf16;
   int mode, gm, shared;
+  int expand;        // Expanded Drop candidates (1 = plain top-1)
   int elem;          // bytes per x/W element
   int BN, BNs;       // token tiles: routed experts, shared expert
   int max_entries;   // N * ceil(C / BN)
@@ -104,6 +105,7 @@ struct Plan {
   int part_units;    // tail-split partial tiles of the tensor-core GEMMs
   // workspace offsets
   bool tc_router;    // bf16 x and N <= kMaxExpertsTc: tensor-core router
+  size_t o_cand, o_candp, o_passcnt, o_used;   // Expanded Drop
   size_t o_Ppart, o_hist, o_rank, o_Psum, o_start, o_list, o_entries, o_ctrl, o_wsplit, o_xbuf,
       o_H0, o_H1, o_O, o_Hs0, o_Hs1, o_Os, o_tok, o_part, o_splitcnt, total;
   // extra for the host-IO entry point
@@ -136,7 +138,10 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
       (p->has_shared != 0 && p->has_shared != 1) ||
       (p->dtype != SWITCH_MOE_F32 && p->dtype != SWITCH_MOE_BF16))
     return SWITCH_MOE_ERR_INVALID_ARG;
+  if (p->expand < 0 || p->expand > kMaxCand) return SWITCH_MOE_ERR_INVALID_ARG;
   if (p->N > kMaxExperts) return SWITCH_MOE_ERR_UNSUPPORTED;
+  if (p->expand > 1 && (p->priority_mode != SWITCH_MOE_TOKEN_ORDER || p->expand > p->N))
+    return SWITCH_MOE_ERR_UNSUPPORTED;
   if (need_gemm && (p->d_model < 8 || p->d_ff < 8 || p->d_model % 8 || p->d_ff % 8))
     return SWITCH_MOE_ERR_UNSUPPORTED;
   if (p->T > (int64_t)1 << 30 || p->d_model > (1 << 20) || p->d_ff > (1 << 20))
@@ -147,6 +152,7 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   q.bf16 = p->dtype == SWITCH_MOE_BF16;
   q.elem = q.bf16 ? 2 : 4;
   q.mode = p->priority_mode; q.gm = p->gate_multiply; q.shared = p->has_shared;
+  q.expand = p->expand > 1 ? p->expand : 1;
   if (q.T == 0) return SWITCH_MOE_OK;
   const int64_t C = capacity_of(q.T, q.N, p->capacity_factor);
   if (C < 1) return SWITCH_MOE_ERR_INVALID_ARG;
@@ -179,6 +185,12 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   q.o_list = take((size_t)q.T * 4);
   q.o_entries = take((size_t)q.max_entries * 8);
   q.o_ctrl = take(64);
+  if (q.expand > 1) {
+    q.o_cand = take((size_t)q.T * kMaxCand * 4);
+    q.o_candp = take((size_t)q.T * kMaxCand * 4);
+    q.o_passcnt = take((size_t)q.N * 4);
+    q.o_used = take((size_t)2 * q.N * 4);   // filled slots, before / after a pass
+  }
   q.tc_router = q.bf16 && q.N <= kMaxExpertsTc;
   if (q.tc_router) q.o_wsplit = take((size_t)3 * router_tc_n_mma((int)q.N) * q.d * 2);
   if (need_gemm) {
@@ -269,6 +281,11 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   ra.expert_id = expert_id; ra.gate = gate;
   ra.P_part = at<float>(ws, q.o_Ppart); ra.hist = at<int32_t>(ws, q.o_hist);
   ra.local_rank = at<int32_t>(ws, q.o_rank); ra.ctrl = ctrl;
+  ra.n_cand = q.expand;
+  if (q.expand > 1) {
+    ra.cand = at<int32_t>(ws, q.o_cand);
+    ra.cand_p = at<float>(ws, q.o_candp);
+  }
   mark(0, s);
   if (x && q.tc_router) {
     int rc = launch_tc_router(q, ra, ws, status, s);
@@ -302,8 +319,35 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   aa.tok_of_slot = (dispatch && q.fused) ? at<int32_t>(ws, q.o_tok) : nullptr;
   aa.y = (dispatch && q.fused && !q.shared) ? y : nullptr;
   aa.status = status;
-  if (launch_assign(aa, sa.defer_finish ? &sa : nullptr, s, true) != cudaSuccess)
+  // with Expanded Drop the work list waits for the last pass (launch_finish)
+  const bool finish_here = sa.defer_finish && q.expand == 1;
+  if (launch_assign(aa, finish_here ? &sa : nullptr, s, true) != cudaSuccess)
     return SWITCH_MOE_ERR_CUDA;
+  if (q.expand > 1) {
+    // passes 2..k: the tokens still unplaced try their next candidate
+    int32_t* used = at<int32_t>(ws, q.o_used);
+    ExpandArgs ea{};
+    ea.T = (int)q.T; ea.N = (int)q.N; ea.C = q.C; ea.d = (int)q.d; ea.elem_bytes = q.elem;
+    ea.cand = ra.cand; ea.cand_p = ra.cand_p; ea.hist = ra.hist; ea.local_rank = ra.local_rank;
+    ea.pass_cnt = at<int32_t>(ws, q.o_passcnt); ea.counts = counts;
+    ea.expert_id = expert_id; ea.gate = gate; ea.slot = slot; ea.drop = drop;
+    ea.x = aa.x; ea.xbuf = aa.xbuf; ea.tok_of_slot = aa.tok_of_slot; ea.status = status;
+    ScanArgs sp = sa;   // the same scan over this pass's histograms
+    sp.counts = at<int32_t>(ws, q.o_passcnt);
+    sp.defer_finish = 1;
+    for (int r = 1; r < q.expand; ++r) {
+      ea.r = r;
+      ea.used_in = r == 1 ? nullptr : used + (size_t)((r + 1) & 1) * q.N;
+      ea.used_out = used + (size_t)(r & 1) * q.N;
+      if (launch_expand_hist(ea, s, true) != cudaSuccess ||
+          launch_scan(sp, s, true) != cudaSuccess ||
+          launch_expand_assign(ea, s, true) != cudaSuccess)
+        return SWITCH_MOE_ERR_CUDA;
+    }
+    // work list from the final filled slots; L_aux from the top-1 counts
+    sa.kept = used + (size_t)((q.expand - 1) & 1) * q.N;
+    if (launch_finish(sa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  }
   if (q.mode == SWITCH_MOE_GATE_PRIORITY) {
     if (launch_gate_select(aa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
     if (dispatch && launch_dispatch(aa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
@@ -434,6 +478,10 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
   int rc = run_routing(q, x, W_g, b_g, nullptr, expert_id, gate, slot, drop, counts, aux, ws,
                        true, y, dev->status, s);
   if (rc) return rc;
+  // filled slots per expert: min(counts, C), or after Expanded Drop its passes' total
+  const int32_t* kept = q.expand > 1
+      ? at<int32_t>(ws, q.o_used) + (size_t)((q.expand - 1) & 1) * q.N
+      : counts;
   void* xbuf = at<void>(ws, q.o_xbuf);
   void* H0 = at<void>(ws, q.o_H0);
   void* H1 = q.bf16 ? at<void>(ws, q.o_H1) : nullptr;
@@ -452,24 +500,24 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
   mark(4, s);
   if (q.ffn) {
     mark(5, s);   // one launch runs both layers
-    if ((rc = run_ffn(q, dev, W1, W2, y, counts, gate, ws, s))) return rc;
+    if ((rc = run_ffn(q, dev, W1, W2, y, kept, gate, ws, s))) return rc;
     mark(6, s);
     mark(7, s);
     return SWITCH_MOE_OK;
   }
-  if ((rc = run_gemm(q, dev, false, 1, W1, xbuf, nullptr, H0, H1, counts, gate, ws, s)))
+  if ((rc = run_gemm(q, dev, false, 1, W1, xbuf, nullptr, H0, H1, kept, gate, ws, s)))
     return rc;
   mark(5, s);
   if (q.fused) {
     // combine runs in the epilogue of the second routed GEMM
-    if ((rc = run_gemm(q, dev, false, 2, W2, H0, H1, y, nullptr, counts, gate, ws, s)))
+    if ((rc = run_gemm(q, dev, false, 2, W2, H0, H1, y, nullptr, kept, gate, ws, s)))
       return rc;
     mark(6, s);
     mark(7, s);
     return SWITCH_MOE_OK;
   }
   float* O = at<float>(ws, q.o_O);
-  if ((rc = run_gemm(q, dev, false, 2, W2, H0, H1, O, nullptr, counts, gate, ws, s))) return rc;
+  if ((rc = run_gemm(q, dev, false, 2, W2, H0, H1, O, nullptr, kept, gate, ws, s))) return rc;
   mark(6, s);
   CombineArgs ca{};
   ca.T = (int)q.T; ca.d = (int)q.d; ca.C = q.C;

@@ -90,8 +90,9 @@ __device__ void finish_experts(const ScanArgs& a, int* sh_i, double* sh_d) {
   for (int i = e0; i < e1; ++i) {
     const int c = __ldcg(a.counts + i);
     const float p = __ldcg(a.P_sum + i);
+    const int kept = a.kept ? __ldcg(a.kept + i) : min(c, a.C);
     c_loc += c;
-    t_loc += (min(c, a.C) + a.BN - 1) / a.BN;
+    t_loc += (kept + a.BN - 1) / a.BN;
     aux_loc += (double)c * (double)p;
   }
   int c_tot, t_tot;
@@ -101,7 +102,8 @@ __device__ void finish_experts(const ScanArgs& a, int* sh_i, double* sh_d) {
     const int c = __ldcg(a.counts + i);
     a.expert_start[i] = c_run;
     c_run += c;
-    const int nt = (min(c, a.C) + a.BN - 1) / a.BN;
+    const int kept = a.kept ? __ldcg(a.kept + i) : min(c, a.C);
+    const int nt = (kept + a.BN - 1) / a.BN;
     for (int j = 0; j < nt; ++j) a.entries[t_run + j] = make_int2(i, j);
     t_run += nt;
   }
@@ -285,6 +287,87 @@ __global__ void __launch_bounds__(kRowWarps * 32) dispatch_kernel(AssignArgs a) 
   if (s < 0 && a.y) zero_row(a.y + (size_t)t * a.d, a.d, lane);
 }
 
+// ------------------------------------------------- Expanded Drop passes
+// Pass r (r = 1..k-1, 0-based candidate index) over the tokens the earlier
+// passes left unplaced, in token order: per 32-token group the histogram of
+// their r-th candidates and each token's rank among earlier same-candidate
+// unplaced tokens of its group; the scan turns the histograms into
+// per-expert exclusive prefixes; a token then takes slot
+// used_e + prefix + rank when that is below C ("MoE 专家容量因子与 Token
+// 丢弃", wiblog.cn, inference section, on Capacity-Aware Inference's
+// Expanded Drop: overflow tokens consider further experts of their
+// candidate set).
+
+__global__ void __launch_bounds__(kRowWarps * 32) expand_hist_kernel(ExpandArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x * kRowWarps + warp;   // 32-token group
+  const int t0 = g * 32;
+  if (t0 >= a.T) return;
+  int32_t* hrow = a.hist + (size_t)g * a.N;
+  for (int i = lane; i < a.N; i += 32) hrow[i] = 0;
+  const int t = t0 + lane;
+  const bool open = t < a.T && a.slot[t] < 0;
+  const int e = open ? a.cand[(size_t)t * kMaxCand + a.r] : -1 - lane;
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  __syncwarp();
+  if (open) {
+    const unsigned lt = (1u << lane) - 1u;
+    a.local_rank[t] = __popc(peers & lt);
+    if ((peers & lt) == 0) hrow[e] = __popc(peers);
+  }
+}
+
+__global__ void __launch_bounds__(kRowWarps * 32) expand_assign_kernel(ExpandArgs a) {
+  extern __shared__ __align__(128) uint8_t rowbuf[];
+  __shared__ __align__(8) uint64_t rowbar[kRowWarps];
+  grid_dep_wait();
+  grid_dep_launch();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto used_before = [&](int e) -> int {
+    return a.used_in ? a.used_in[e] : min(a.counts[e], a.C);
+  };
+  if (blockIdx.x == gridDim.x - 1) {   // the extra CTA: filled slots after this pass
+    for (int e = threadIdx.x; e < a.N; e += blockDim.x)
+      a.used_out[e] = min(a.C, used_before(e) + a.pass_cnt[e]);
+    return;
+  }
+  const int t = blockIdx.x * kRowWarps + warp;
+  if (t >= a.T || a.slot[t] >= 0) return;
+  const int e = a.cand[(size_t)t * kMaxCand + a.r];
+  const int s = used_before(e) + a.hist[(size_t)(t / 32) * a.N + e] + a.local_rank[t];
+  if (s >= a.C) return;   // this candidate is full too
+  if (lane == 0) {
+    a.slot[t] = s;
+    a.drop[t] = 0;
+    a.expert_id[t] = e;
+    a.gate[t] = a.cand_p[(size_t)t * kMaxCand + a.r];
+    if (a.xbuf && a.tok_of_slot) a.tok_of_slot[(size_t)e * a.C + s] = t;
+  }
+  if (a.xbuf) {
+    const uint32_t rb = (uint32_t)a.d * (uint32_t)a.elem_bytes;
+    if (rb <= kStageRowMax) {
+      AssignArgs aa{};
+      aa.x = a.x; aa.xbuf = a.xbuf; aa.C = a.C; aa.status = a.status;
+      uint8_t* buf = rowbuf + (size_t)warp * rb;
+      stage_row_begin(aa, buf, &rowbar[warp], t, rb, lane);
+      stage_row_end(aa, buf, &rowbar[warp], e, s, rb, lane);
+    } else {
+      copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
+               static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads) finish_kernel(ScanArgs a) {
+  __shared__ int sh_i[33];
+  __shared__ double sh_d[32];
+  grid_dep_wait();
+  grid_dep_launch();
+  finish_experts(a, sh_i, sh_d);
+}
+
 constexpr int kSelThreads = 1024;
 
 __device__ __forceinline__ unsigned long long gate_key(const AssignArgs& a, int t) {
@@ -429,6 +512,30 @@ cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s, bool pdl) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   return launch_k(gate_select_kernel, dim3(a.N), dim3(kSelThreads), smem, s, pdl, a);
+}
+
+}  // namespace smoe
+
+namespace smoe {
+
+cudaError_t launch_expand_hist(const ExpandArgs& a, cudaStream_t s, bool pdl) {
+  const int groups = (a.T + 31) / 32;
+  return launch_k(expand_hist_kernel, dim3((groups + kRowWarps - 1) / kRowWarps),
+                  dim3(kRowWarps * 32), 0, s, pdl, a);
+}
+
+cudaError_t launch_expand_assign(const ExpandArgs& a, cudaStream_t s, bool pdl) {
+  const size_t rb = (size_t)a.d * a.elem_bytes;
+  const size_t smem = (a.xbuf && rb <= kStageRowMax) ? (size_t)kRowWarps * rb : 0;
+  cudaError_t err = cudaFuncSetAttribute(expand_assign_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  return launch_k(expand_assign_kernel, dim3((a.T + kRowWarps - 1) / kRowWarps + 1),
+                  dim3(kRowWarps * 32), smem, s, pdl, a);
+}
+
+cudaError_t launch_finish(const ScanArgs& a, cudaStream_t s, bool pdl) {
+  return launch_k(finish_kernel, dim3(1), dim3(kScanThreads), 0, s, pdl, a);
 }
 
 }  // namespace smoe

@@ -37,6 +37,7 @@ constexpr int kTileM = 128;          // weight rows per tensor-core tile (MMA M)
 constexpr int kTileK = 64;           // bf16 elements per 128-byte K block
 constexpr int kSimtTileN = 32;       // tokens per fp32 SIMT tile
 constexpr int kMaxExpertsTc = 256;   // experts the tensor-core router takes (one MMA N)
+constexpr int kMaxCand = 4;          // Expanded Drop: candidates per token
 
 // ------------------------------------------------------------------ router
 struct RouterArgs {
@@ -54,7 +55,33 @@ struct RouterArgs {
   int32_t* hist;          // [R, N]  per-CTA expert histograms (scanned in place later)
   int32_t* local_rank;    // [T]     rank of the token among same-expert tokens of its CTA
   int32_t* ctrl;          // control words (zeroed by CTA 0)
+  // Expanded Drop: n_cand > 1 also stores each token's first n_cand experts
+  // by logit (lowest index first on ties) and their probabilities
+  int n_cand;
+  int32_t* cand;          // [T][kMaxCand]
+  float* cand_p;          // [T][kMaxCand]
 };
+
+// Candidates 2..k of a token: the experts with the next highest logits in
+// turn, lowest index first among equal logits (strict comparison in
+// increasing index), skipping those already taken.  at(i) is logit i.
+template <typename At>
+__device__ __forceinline__ void next_candidates(At at, int N, int k, int (&cand)[kMaxCand]) {
+  for (int r = 1; r < k; ++r) {
+    float best = 0.f;
+    int bi = -1;
+    for (int i = 0; i < N; ++i) {
+      bool taken = false;
+      for (int q = 0; q < r; ++q) taken |= cand[q] == i;
+      const float v = at(i);
+      if (!taken && (bi < 0 || v > best)) {
+        best = v;
+        bi = i;
+      }
+    }
+    cand[r] = bi;
+  }
+}
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 // bf16 layers with N <= kMaxExpertsTc: W_g split into three bf16 pieces
 // [3][n_mma][d] (rows >= N zero), then the tensor-core router over them.
@@ -81,6 +108,9 @@ struct ScanArgs {
   // 1: the scan stores counts / probability sums only; finish_experts (prefix,
   // work list, L_aux) runs in an extra CTA of the slot-assignment kernel
   int defer_finish;
+  // filled slots per expert for the work list (Expanded Drop), or null:
+  // min(counts, C)
+  const int32_t* kept;
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl = false);
 
@@ -114,6 +144,36 @@ cudaError_t launch_assign(const AssignArgs& a, const ScanArgs* finish, cudaStrea
 cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s, bool pdl = false);
 // Copy kept rows x[t] -> xbuf[e * C + slot[t]] (gate-priority path).
 cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s, bool pdl = false);
+
+// ------------------------------------------- Expanded Drop, passes 2..k
+struct ExpandArgs {
+  int T, N, C, d, elem_bytes;
+  int r;                       // candidate index of this pass (1..k-1)
+  const int32_t* cand;         // [T][kMaxCand]
+  const float* cand_p;         // [T][kMaxCand]
+  int32_t* hist;               // [R, N] this pass's group histograms (scanned in place)
+  int32_t* local_rank;         // [T]
+  const int32_t* pass_cnt;     // [N] this pass's per-expert totals (from the scan)
+  const int32_t* counts;       // [N] top-1 counts (first expand pass: used = min(counts, C))
+  const int32_t* used_in;      // [N] filled slots before this pass (null on the first)
+  int32_t* used_out;           // [N] filled slots after this pass
+  int32_t* expert_id;          // [T] updated for re-routed tokens
+  float* gate;
+  int32_t* slot;
+  uint8_t* drop;
+  const void* x;               // null: routing only
+  void* xbuf;
+  int32_t* tok_of_slot;        // [N * C] or null
+  int* status;
+};
+// Per 32-token group: histogram and in-group ranks of the still-unplaced
+// tokens' r-th candidates.
+cudaError_t launch_expand_hist(const ExpandArgs& a, cudaStream_t s, bool pdl);
+// Place still-unplaced tokens on their r-th candidate when it has room;
+// one extra CTA writes used_out.
+cudaError_t launch_expand_assign(const ExpandArgs& a, cudaStream_t s, bool pdl);
+// finish_experts alone (one CTA), after the last Expanded Drop pass.
+cudaError_t launch_finish(const ScanArgs& a, cudaStream_t s, bool pdl);
 
 // ------------------------------------------------------- expert GEMMs
 // D[e, m, c] = sum_k A[e * M + m, k] * B[e * rows + nt * BN + c, k] for the

@@ -121,10 +121,16 @@ __device__ void route_tile(float* lg, int ldl, int T, int N, int t0, int cta,
     float s = 0.f;
     for (int i = 0; i < N; ++i) s += expf(row[i] - m);
     const float inv = 1.0f / s;
+    int cand[kMaxCand] = {mi, 0, 0, 0};
+    if (a.n_cand > 1) next_candidates([&](int i) { return row[i]; }, N, a.n_cand, cand);
     for (int i = 0; i < N; ++i) row[i] = expf(row[i] - m) * inv;   // probabilities
     a.expert_id[t] = mi;
     a.gate[t] = inv;    // score of the argmax: exp(0) / s
     es[tid] = mi;
+    for (int r = 0; r < a.n_cand && a.n_cand > 1; ++r) {
+      a.cand[(size_t)t * kMaxCand + r] = cand[r];
+      a.cand_p[(size_t)t * kMaxCand + r] = row[cand[r]];
+    }
   }
   for (int i = tid; i < N; i += NTHREADS) hs[i] = 0;
   __syncthreads();

@@ -105,6 +105,8 @@ __device__ __noinline__ void route_group_smem(const RouterArgs& a, float* lg, fl
       mi = i;
     }
   }
+  int cand[kMaxCand] = {mi, 0, 0, 0};
+  if (a.n_cand > 1) next_candidates([&](int i) { return row[i]; }, N, a.n_cand, cand);
   float s = 0.f;
   for (int i = 0; i < N; ++i) {
     const float e = expf(row[i] - m);
@@ -116,6 +118,10 @@ __device__ __noinline__ void route_group_smem(const RouterArgs& a, float* lg, fl
   if (valid) {
     a.expert_id[t] = mi;
     a.gate[t] = inv;   // exp(0) / s: the probability of the argmax
+    for (int c = 0; c < a.n_cand && a.n_cand > 1; ++c) {
+      a.cand[(size_t)t * kMaxCand + c] = cand[c];
+      a.cand_p[(size_t)t * kMaxCand + c] = row[cand[c]] * inv;   // exp(l - m) / s
+    }
   }
   __syncwarp();
   const int nvalid = min(32, T - (t0 + q * 32));
@@ -413,6 +419,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!a.logits_out && valid) {
         a.expert_id[t] = mi;
         a.gate[t] = inv;
+      }
+      if (!a.logits_out && a.n_cand > 1) {
+        // Expanded Drop candidates: next highest logits in turn (lowest index
+        // on ties), one more pass over the TMEM row each
+        int cand[kMaxCand] = {mi, 0, 0, 0};
+        float cl[kMaxCand] = {m, 0.f, 0.f, 0.f};
+        for (int r = 1; r < a.n_cand; ++r) {
+          float best = 0.f;
+          int bi = -1;
+          for (int c0 = 0; c0 < N; c0 += 16) {
+            tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int i = c0 + j;
+              bool taken = i >= N;
+              for (int qq = 0; qq < r; ++qq) taken |= cand[qq] == i;
+              const float l = v[j] + bias_s[min(i, N - 1)];
+              if (!taken && (bi < 0 || l > best)) {
+                best = l;
+                bi = i;
+              }
+            }
+          }
+          cand[r] = bi;
+          cl[r] = best;
+        }
+        if (valid) {
+          for (int r = 0; r < a.n_cand; ++r) {
+            a.cand[(size_t)t * kMaxCand + r] = cand[r];
+            a.cand_p[(size_t)t * kMaxCand + r] = expf(cl[r] - m) * inv;
+          }
+        }
       }
       // pass 3, 32 experts at a time: probabilities through this warp's
       // [32][33] slice of the (now idle) pipeline buffers, then the group's
