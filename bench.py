@@ -165,10 +165,11 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle sample
-def oracle_sample_step(w, seed=0):
-    """One bounded CPU-oracle step on the workload: route the whole batch,
-    then the expert FFN and combine of the tokens routed to the first
-    CPU_SAMPLE_EXPERTS experts.  Returns (tokens processed, seconds)."""
+def oracle_sample_step(w, seed=0, expand=1):
+    """One bounded CPU-oracle step on the workload: route the whole batch
+    (with Expanded Drop over `expand` candidates when > 1), then the expert
+    FFN and combine of the tokens processed by the first CPU_SAMPLE_EXPERTS
+    experts.  Returns (tokens processed, seconds)."""
     import oracle
     inp = make_inputs(w, seed, device="cpu", with_experts=False)
     experts = {e: expert_weights(w, e, seed, "cpu") for e in range(min(CPU_SAMPLE_EXPERTS, w.N))}
@@ -176,9 +177,14 @@ def oracle_sample_step(w, seed=0):
     r = oracle.route(inp.x, inp.W_g, zipf_bias(w))
     C = oracle.capacity(w.T, w.N, w.capacity_factor)
     slot, drop, counts = oracle.assign_slots(r["expert_id"], r["gate"], w.N, C, w.priority_mode)
-    rows = np.nonzero(r["expert_id"] < len(experts))[0]
-    oracle.forward_rows(rows, inp.x, r["expert_id"], r["gate"], slot, w.gate_multiply,
-                        lambda e: experts[e], inp.W1s, inp.W2s)
+    e, g = r["expert_id"], r["gate"]
+    if expand > 1:
+        e, slot, drop, _ = oracle.assign_slots_expanded(oracle.candidates(r["logits"], expand),
+                                                        w.N, C)
+        g = r["probs"][np.arange(w.T), e]
+    rows = np.nonzero(e < len(experts))[0]
+    oracle.forward_rows(rows, inp.x, e, g, slot, w.gate_multiply,
+                        lambda i: experts[i], inp.W1s, inp.W2s)
     oracle.aux_loss(r["probs"], counts)
     return int(rows.size), time.perf_counter() - t0
 
@@ -202,13 +208,15 @@ def cpu_sample_desc(w):
 
 def run_reference(args, rank, world):
     w = CONFIGS[args.config]
+    if args.token_order:
+        w = w.replace(priority_mode=0)
     if rank != 0:
         return
     for _ in range(args.warmup):
-        oracle_sample_step(w)
+        oracle_sample_step(w, expand=args.expand)
     tok, sec = 0, 0.0
     for _ in range(args.steps):
-        n, s = oracle_sample_step(w)
+        n, s = oracle_sample_step(w, expand=args.expand)
         tok += n
         sec += s
     value = tok / sec
@@ -218,7 +226,7 @@ def run_reference(args, rank, world):
         "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w),
+        "config": workload_config(w, args.expand),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": cpu_sample_desc(w)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -227,10 +235,12 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w):
+def workload_config(w, expand=1):
     return {"workload": f"{w.name}: Switch top-1 MoE layer T={w.T} d_model={w.d_model} "
                         f"d_ff={w.d_ff} N={w.N} cf={w.capacity_factor} {w.dtype}"
-                        f"{' +shared expert' if w.has_shared else ''}",
+                        f"{' +shared expert' if w.has_shared else ''}"
+                        f"{f' +Expanded Drop over {expand} candidates' if expand > 1 else ''}",
+            "expanded_drop_candidates": expand,
             "T": w.T, "d_model": w.d_model, "d_ff": w.d_ff, "N": w.N,
             "capacity_factor": w.capacity_factor,
             "priority": "gate" if w.priority_mode else "token-order",
@@ -249,6 +259,11 @@ def main():
     ap.add_argument("--config", default="base", choices=sorted(CONFIGS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--expand", type=int, default=1,
+                    help="Expanded Drop: candidates per token (1 = plain top-1)")
+    ap.add_argument("--token-order", action="store_true",
+                    help="token-order priority whatever the workload's (Expanded Drop "
+                         "on the skewed shape)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -269,9 +284,12 @@ def main():
         pg = dist
 
     w = CONFIGS[args.config]
+    if args.token_order:
+        w = w.replace(priority_mode=0)
     inp = make_inputs(w, seed=0, device=dev)
     p = sm.make_params(w.T, w.d_model, w.d_ff, w.N, w.capacity_factor, w.priority_mode,
-                       w.gate_multiply, sm.BF16 if w.dtype == "bf16" else sm.F32, w.has_shared)
+                       w.gate_multiply, sm.BF16 if w.dtype == "bf16" else sm.F32, w.has_shared,
+                       args.expand)
     ws = sm.workspace(sm.switch_moe_workspace_bytes(p), dev)
     out = None
     stream = torch.cuda.current_stream(dev)
@@ -280,7 +298,8 @@ def main():
         nonlocal out
         out = sm.switch_moe_forward(inp.x, inp.W_g, inp.W1, inp.W2, w.capacity_factor,
                                     w.priority_mode, w.gate_multiply, b_g=inp.b_g,
-                                    W1s=inp.W1s, W2s=inp.W2s, ws=ws, out=out)
+                                    W1s=inp.W1s, W2s=inp.W2s, ws=ws, out=out,
+                                    expand=args.expand)
 
     for _ in range(args.warmup):
         step()
@@ -328,9 +347,11 @@ def main():
                 for i, name in enumerate(sm.PHASES)}
 
     # ---- workload facts for the roofline
-    counts = out.expert_counts.cpu().numpy().astype(np.int64)
     C = sm.switch_moe_capacity(w.T, w.N, w.capacity_factor)
-    kept = np.minimum(counts, C)
+    # filled slots per expert (with Expanded Drop, re-routed tokens count
+    # for the expert that runs them)
+    eid, slt = out.expert_id.cpu().numpy(), out.slot.cpu().numpy()
+    kept = np.bincount(eid[slt >= 0], minlength=w.N).astype(np.int64)
     active = int((kept > 0).sum())
     T_kept = int(kept.sum())
     eb = 2 if w.dtype == "bf16" else 4
@@ -358,7 +379,8 @@ def main():
     # ranking + dispatch], GEMM 1 [+ shared GEMMs], GEMM 2 [+ combine when the
     # second GEMM's epilogue cannot do it: fp32 layers, K-split GEMM 2]
     launches = ((2 if tc_router else 1) + 2 + (2 if w.priority_mode else 0)
-                + (1 if ffn_one else 2) + (2 if w.has_shared else 0) + (0 if fused else 1))
+                + (1 if ffn_one else 2) + (2 if w.has_shared else 0) + (0 if fused else 1)
+                + (3 * (args.expand - 1) + 1 if args.expand > 1 else 0))
 
     # ---- end to end through the host-buffer entry point
     e2e = None
@@ -372,7 +394,8 @@ def main():
             hout = sm.switch_moe_forward_hostio(x_host, inp.W_g, inp.W1, inp.W2,
                                                 w.capacity_factor, w.priority_mode,
                                                 w.gate_multiply, b_g=inp.b_g, W1s=inp.W1s,
-                                                W2s=inp.W2s, ws=hws, out=hout)
+                                                W2s=inp.W2s, ws=hws, out=hout,
+                                                expand=args.expand)
         for _ in range(args.warmup):
             hstep()
         torch.cuda.synchronize()
@@ -397,7 +420,7 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tok, sec = 0, 0.0
         while sec < 10.0:
-            n, s = oracle_sample_step(w)
+            n, s = oracle_sample_step(w, expand=args.expand)
             tok += n
             sec += s
         cpu = {"value": tok / sec, "unit": "tokens/s", "cores": blas_threads(),
@@ -409,7 +432,7 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": workload_config(w),
+            "config": workload_config(w, args.expand),
             "e2e": e2e,
             "roofline": {"kernel": ("ffn_tc_kernel (expert GEMM 1 + 2, one launch)" if ffn_one
                                     else "gemm_tc_kernel (expert GEMM 1 + 2)"),

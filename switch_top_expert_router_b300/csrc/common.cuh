@@ -62,24 +62,36 @@ struct RouterArgs {
   float* cand_p;          // [T][kMaxCand]
 };
 
-// Candidates 2..k of a token: the experts with the next highest logits in
-// turn, lowest index first among equal logits (strict comparison in
-// increasing index), skipping those already taken.  at(i) is logit i.
+// A token's first kMaxCand experts by logit, descending, lowest index first
+// among equal logits, in one pass over its N logits (at(i) is logit i):
+// insertion into a sorted list of kMaxCand.  A logit goes in above the first
+// entry it strictly exceeds (an equal logit stays behind the earlier index)
+// and every entry from there on moves down one place.  cand[0] is the top-1
+// expert (the first maximum).
 template <typename At>
-__device__ __forceinline__ void next_candidates(At at, int N, int k, int (&cand)[kMaxCand]) {
-  for (int r = 1; r < k; ++r) {
-    float best = 0.f;
-    int bi = -1;
-    for (int i = 0; i < N; ++i) {
-      bool taken = false;
-      for (int q = 0; q < r; ++q) taken |= cand[q] == i;
-      const float v = at(i);
-      if (!taken && (bi < 0 || v > best)) {
-        best = v;
-        bi = i;
+__device__ __forceinline__ void topk_candidates(At at, int N, int (&cand)[kMaxCand],
+                                                float (&cv)[kMaxCand]) {
+#pragma unroll
+  for (int q = 0; q < kMaxCand; ++q) {
+    cand[q] = -1;
+    cv[q] = 0.f;
+  }
+  for (int i = 0; i < N; ++i) {
+    float nv = at(i);
+    int ni = i;
+    bool moved = false;
+#pragma unroll
+    for (int q = 0; q < kMaxCand; ++q) {
+      if (moved || cand[q] < 0 || nv > cv[q]) {
+        const float tv = cv[q];
+        const int ti = cand[q];
+        cv[q] = nv;
+        cand[q] = ni;
+        nv = tv;
+        ni = ti;
+        moved = true;
       }
     }
-    cand[r] = bi;
   }
 }
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);

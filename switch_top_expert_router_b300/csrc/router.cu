@@ -121,8 +121,9 @@ __device__ void route_tile(float* lg, int ldl, int T, int N, int t0, int cta,
     float s = 0.f;
     for (int i = 0; i < N; ++i) s += expf(row[i] - m);
     const float inv = 1.0f / s;
-    int cand[kMaxCand] = {mi, 0, 0, 0};
-    if (a.n_cand > 1) next_candidates([&](int i) { return row[i]; }, N, a.n_cand, cand);
+    int cand[kMaxCand];
+    float cv[kMaxCand];
+    if (a.n_cand > 1) topk_candidates([&](int i) { return row[i]; }, N, cand, cv);
     for (int i = 0; i < N; ++i) row[i] = expf(row[i] - m) * inv;   // probabilities
     a.expert_id[t] = mi;
     a.gate[t] = inv;    // score of the argmax: exp(0) / s

@@ -105,8 +105,9 @@ __device__ __noinline__ void route_group_smem(const RouterArgs& a, float* lg, fl
       mi = i;
     }
   }
-  int cand[kMaxCand] = {mi, 0, 0, 0};
-  if (a.n_cand > 1) next_candidates([&](int i) { return row[i]; }, N, a.n_cand, cand);
+  int cand[kMaxCand];
+  float cv[kMaxCand];
+  if (a.n_cand > 1) topk_candidates([&](int i) { return row[i]; }, N, cand, cv);
   float s = 0.f;
   for (int i = 0; i < N; ++i) {
     const float e = expf(row[i] - m);
@@ -421,29 +422,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.gate[t] = inv;
       }
       if (!a.logits_out && a.n_cand > 1) {
-        // Expanded Drop candidates: next highest logits in turn (lowest index
-        // on ties), one more pass over the TMEM row each
-        int cand[kMaxCand] = {mi, 0, 0, 0};
-        float cl[kMaxCand] = {m, 0.f, 0.f, 0.f};
-        for (int r = 1; r < a.n_cand; ++r) {
-          float best = 0.f;
-          int bi = -1;
-          for (int c0 = 0; c0 < N; c0 += 16) {
-            tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
+        // Expanded Drop candidates: one more pass over the TMEM row with the
+        // insertion of topk_candidates
+        int cand[kMaxCand];
+        float cl[kMaxCand];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int i = c0 + j;
-              bool taken = i >= N;
-              for (int qq = 0; qq < r; ++qq) taken |= cand[qq] == i;
-              const float l = v[j] + bias_s[min(i, N - 1)];
-              if (!taken && (bi < 0 || l > best)) {
-                best = l;
-                bi = i;
+        for (int qq = 0; qq < kMaxCand; ++qq) {
+          cand[qq] = -1;
+          cl[qq] = 0.f;
+        }
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          tmem_ld_32x32b_x16(taddr + (uint32_t)c0, v);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int i = c0 + j;
+            if (i >= N) continue;
+            float nv = v[j] + bias_s[i];
+            int ni = i;
+            bool moved = false;
+#pragma unroll
+            for (int qq = 0; qq < kMaxCand; ++qq) {
+              if (moved || cand[qq] < 0 || nv > cl[qq]) {
+                const float tv = cl[qq];
+                const int ti = cand[qq];
+                cl[qq] = nv;
+                cand[qq] = ni;
+                nv = tv;
+                ni = ti;
+                moved = true;
               }
             }
           }
-          cand[r] = bi;
-          cl[r] = best;
         }
         if (valid) {
           for (int r = 0; r < a.n_cand; ++r) {
