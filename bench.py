@@ -378,9 +378,10 @@ def main():
     # kernels per forward: [split W_g +] router, scan, slots/dispatch [+ gate
     # ranking + dispatch], GEMM 1 [+ shared GEMMs], GEMM 2 [+ combine when the
     # second GEMM's epilogue cannot do it: fp32 layers, K-split GEMM 2]
+    # [+ Expanded Drop passes and the moved rows' dispatch]
     launches = ((2 if tc_router else 1) + 2 + (2 if w.priority_mode else 0)
                 + (1 if ffn_one else 2) + (2 if w.has_shared else 0) + (0 if fused else 1)
-                + (3 * (args.expand - 1) + 1 if args.expand > 1 else 0))
+                + (2 if args.expand > 1 else 0))
 
     # ---- end to end through the host-buffer entry point
     e2e = None

@@ -105,7 +105,7 @@ struct Plan {
   int part_units;    // tail-split partial tiles of the tensor-core GEMMs
   // workspace offsets
   bool tc_router;    // bf16 x and N <= kMaxExpertsTc: tensor-core router
-  size_t o_cand, o_candp, o_passcnt, o_used;   // Expanded Drop
+  size_t o_cand, o_candp, o_used;   // Expanded Drop
   size_t o_Ppart, o_hist, o_rank, o_Psum, o_start, o_list, o_entries, o_ctrl, o_wsplit, o_xbuf,
       o_H0, o_H1, o_O, o_Hs0, o_Hs1, o_Os, o_tok, o_part, o_splitcnt, total;
   // extra for the host-IO entry point
@@ -188,8 +188,7 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   if (q.expand > 1) {
     q.o_cand = take((size_t)q.T * kMaxCand * 4);
     q.o_candp = take((size_t)q.T * kMaxCand * 4);
-    q.o_passcnt = take((size_t)q.N * 4);
-    q.o_used = take((size_t)2 * q.N * 4);   // filled slots, before / after a pass
+    q.o_used = take((size_t)q.N * 4);   // filled slots after the last pass
   }
   q.tc_router = q.bf16 && q.N <= kMaxExpertsTc;
   if (q.tc_router) q.o_wsplit = take((size_t)3 * router_tc_n_mma((int)q.N) * q.d * 2);
@@ -319,34 +318,25 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   aa.tok_of_slot = (dispatch && q.fused) ? at<int32_t>(ws, q.o_tok) : nullptr;
   aa.y = (dispatch && q.fused && !q.shared) ? y : nullptr;
   aa.status = status;
-  // with Expanded Drop the work list waits for the last pass (launch_finish)
+  // with Expanded Drop the work list waits for the last pass (launch_expand)
   const bool finish_here = sa.defer_finish && q.expand == 1;
   if (launch_assign(aa, finish_here ? &sa : nullptr, s, true) != cudaSuccess)
     return SWITCH_MOE_ERR_CUDA;
   if (q.expand > 1) {
-    // passes 2..k: the tokens still unplaced try their next candidate
-    int32_t* used = at<int32_t>(ws, q.o_used);
+    // passes 2..k: the tokens still unplaced try their next candidate; the
+    // work list and L_aux follow in the same CTA, then the moved rows' copies
     ExpandArgs ea{};
     ea.T = (int)q.T; ea.N = (int)q.N; ea.C = q.C; ea.d = (int)q.d; ea.elem_bytes = q.elem;
-    ea.cand = ra.cand; ea.cand_p = ra.cand_p; ea.hist = ra.hist; ea.local_rank = ra.local_rank;
-    ea.pass_cnt = at<int32_t>(ws, q.o_passcnt); ea.counts = counts;
+    ea.k = q.expand; ea.cand = ra.cand; ea.cand_p = ra.cand_p; ea.counts = counts;
+    ea.open = aa.sorted_list;      // unused by token order
+    ea.moved = ra.local_rank;      // read by the top-1 pass only
+    ea.n_moved = ctrl + 2;
+    ea.used = at<int32_t>(ws, q.o_used);
     ea.expert_id = expert_id; ea.gate = gate; ea.slot = slot; ea.drop = drop;
-    ea.x = aa.x; ea.xbuf = aa.xbuf; ea.tok_of_slot = aa.tok_of_slot; ea.status = status;
-    ScanArgs sp = sa;   // the same scan over this pass's histograms
-    sp.counts = at<int32_t>(ws, q.o_passcnt);
-    sp.defer_finish = 1;
-    for (int r = 1; r < q.expand; ++r) {
-      ea.r = r;
-      ea.used_in = r == 1 ? nullptr : used + (size_t)((r + 1) & 1) * q.N;
-      ea.used_out = used + (size_t)(r & 1) * q.N;
-      if (launch_expand_hist(ea, s, true) != cudaSuccess ||
-          launch_scan(sp, s, true) != cudaSuccess ||
-          launch_expand_assign(ea, s, true) != cudaSuccess)
-        return SWITCH_MOE_ERR_CUDA;
-    }
-    // work list from the final filled slots; L_aux from the top-1 counts
-    sa.kept = used + (size_t)((q.expand - 1) & 1) * q.N;
-    if (launch_finish(sa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+    ea.tok_of_slot = aa.tok_of_slot; ea.x = aa.x; ea.xbuf = aa.xbuf;
+    sa.kept = ea.used;
+    if (launch_expand(ea, sa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+    if (ea.xbuf && launch_expand_dispatch(ea, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   }
   if (q.mode == SWITCH_MOE_GATE_PRIORITY) {
     if (launch_gate_select(aa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
@@ -479,9 +469,7 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
                        true, y, dev->status, s);
   if (rc) return rc;
   // filled slots per expert: min(counts, C), or after Expanded Drop its passes' total
-  const int32_t* kept = q.expand > 1
-      ? at<int32_t>(ws, q.o_used) + (size_t)((q.expand - 1) & 1) * q.N
-      : counts;
+  const int32_t* kept = q.expand > 1 ? at<int32_t>(ws, q.o_used) : counts;
   void* xbuf = at<void>(ws, q.o_xbuf);
   void* H0 = at<void>(ws, q.o_H0);
   void* H1 = q.bf16 ? at<void>(ws, q.o_H1) : nullptr;

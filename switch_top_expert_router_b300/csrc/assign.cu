@@ -31,7 +31,7 @@ namespace {
 
 constexpr int kScanThreads = 256;
 
-// Exclusive scan of one int per thread across the block (kScanThreads).
+// Exclusive scan of one int per thread across the block (up to 1024 threads).
 __device__ int block_exclusive_scan(int v, int* total, int* sh /*[32]*/) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int inc = v;
@@ -83,33 +83,43 @@ __device__ F block_sum(F v, F* sh /*[32]*/) {
 __device__ void finish_experts(const ScanArgs& a, int* sh_i, double* sh_d) {
   const int tid = threadIdx.x;
   // Each thread owns a contiguous run of up to 4 experts.
-  const int per_e = (a.N + kScanThreads - 1) / kScanThreads;   // <= 4 for N <= 1024
+  const int per_e = (a.N + (int)blockDim.x - 1) / (int)blockDim.x;   // <= 4 for N <= 1024
   const int e0 = min(a.N, tid * per_e), e1 = min(a.N, e0 + per_e);
   int c_loc = 0, t_loc = 0;
   double aux_loc = 0.0;
-  for (int i = e0; i < e1; ++i) {
-    const int c = __ldcg(a.counts + i);
-    const float p = __ldcg(a.P_sum + i);
-    const int kept = a.kept ? __ldcg(a.kept + i) : min(c, a.C);
-    c_loc += c;
-    t_loc += (kept + a.BN - 1) / a.BN;
-    aux_loc += (double)c * (double)p;
+  int cv[4], nv[4];   // this thread's counts and token tiles, loaded once
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = e0 + j;
+    cv[j] = 0;
+    nv[j] = 0;
+    if (i < e1) {
+      const int c = __ldcg(a.counts + i);
+      const float p = __ldcg(a.P_sum + i);
+      const int kept = a.kept ? __ldcg(a.kept + i) : min(c, a.C);
+      cv[j] = c;
+      nv[j] = (kept + a.BN - 1) / a.BN;
+      c_loc += c;
+      t_loc += nv[j];
+      aux_loc += (double)c * (double)p;
+    }
   }
   int c_tot, t_tot;
   int c_run = block_exclusive_scan(c_loc, &c_tot, sh_i);
   int t_run = block_exclusive_scan(t_loc, &t_tot, sh_i);
-  for (int i = e0; i < e1; ++i) {
-    const int c = __ldcg(a.counts + i);
-    a.expert_start[i] = c_run;
-    c_run += c;
-    const int kept = a.kept ? __ldcg(a.kept + i) : min(c, a.C);
-    const int nt = (kept + a.BN - 1) / a.BN;
-    for (int j = 0; j < nt; ++j) a.entries[t_run + j] = make_int2(i, j);
-    t_run += nt;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = e0 + j;
+    if (i < e1) {
+      a.expert_start[i] = c_run;
+      c_run += cv[j];
+      for (int q = 0; q < nv[j]; ++q) a.entries[t_run + q] = make_int2(i, q);
+      t_run += nv[j];
+    }
   }
   const double aux = block_sum<double>(aux_loc, sh_d);
   if (a.split_cnt)
-    for (int i = tid; i < a.n_split_cnt; i += kScanThreads) a.split_cnt[i] = 0;
+    for (int i = tid; i < a.n_split_cnt; i += blockDim.x) a.split_cnt[i] = 0;
   if (tid == 0) {
     a.expert_start[a.N] = c_tot;
     a.ctrl[1] = t_tot;
@@ -288,84 +298,141 @@ __global__ void __launch_bounds__(kRowWarps * 32) dispatch_kernel(AssignArgs a) 
 }
 
 // ------------------------------------------------- Expanded Drop passes
-// Pass r (r = 1..k-1, 0-based candidate index) over the tokens the earlier
-// passes left unplaced, in token order: per 32-token group the histogram of
-// their r-th candidates and each token's rank among earlier same-candidate
-// unplaced tokens of its group; the scan turns the histograms into
-// per-expert exclusive prefixes; a token then takes slot
-// used_e + prefix + rank when that is below C ("MoE 专家容量因子与 Token
-// 丢弃", wiblog.cn, inference section, on Capacity-Aware Inference's
-// Expanded Drop: overflow tokens consider further experts of their
-// candidate set).
+// After the top-1 pass, pass r (r = 2..k) runs over the tokens still
+// unplaced, in token order: each tries its r-th candidate and takes that
+// expert's next free slot while one is left ("MoE 专家容量因子与 Token 丢弃",
+// wiblog.cn, inference section, on Capacity-Aware Inference's Expanded
+// Drop: overflow tokens consider further experts of their candidate set).
+// The processing expert's probability becomes the token's gate.
+//
+// One CTA of kExpandThreads: the unplaced tokens are few and every pass
+// depends on the one before, so the CTA walks them in chunks of 1024.  In
+// a chunk each token's slot is fill[e] + (same-candidate tokens of earlier
+// warps) + (rank among its warp's same-candidate tokens); the last group of
+// each expert in the chunk advances fill[e].  Tokens left over are compacted
+// in order for the next pass.
 
-__global__ void __launch_bounds__(kRowWarps * 32) expand_hist_kernel(ExpandArgs a) {
-  grid_dep_wait();
-  grid_dep_launch();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.x * kRowWarps + warp;   // 32-token group
-  const int t0 = g * 32;
-  if (t0 >= a.T) return;
-  int32_t* hrow = a.hist + (size_t)g * a.N;
-  for (int i = lane; i < a.N; i += 32) hrow[i] = 0;
-  const int t = t0 + lane;
-  const bool open = t < a.T && a.slot[t] < 0;
-  const int e = open ? a.cand[(size_t)t * kMaxCand + a.r] : -1 - lane;
-  const unsigned peers = __match_any_sync(0xffffffffu, e);
-  __syncwarp();
-  if (open) {
-    const unsigned lt = (1u << lane) - 1u;
-    a.local_rank[t] = __popc(peers & lt);
-    if ((peers & lt) == 0) hrow[e] = __popc(peers);
-  }
-}
+constexpr int kExpandThreads = 1024;
+constexpr int kExpandWarps = kExpandThreads / 32;
 
-__global__ void __launch_bounds__(kRowWarps * 32) expand_assign_kernel(ExpandArgs a) {
-  extern __shared__ __align__(128) uint8_t rowbuf[];
-  __shared__ __align__(8) uint64_t rowbar[kRowWarps];
-  grid_dep_wait();
-  grid_dep_launch();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  auto used_before = [&](int e) -> int {
-    return a.used_in ? a.used_in[e] : min(a.counts[e], a.C);
-  };
-  if (blockIdx.x == gridDim.x - 1) {   // the extra CTA: filled slots after this pass
-    for (int e = threadIdx.x; e < a.N; e += blockDim.x)
-      a.used_out[e] = min(a.C, used_before(e) + a.pass_cnt[e]);
-    return;
-  }
-  const int t = blockIdx.x * kRowWarps + warp;
-  if (t >= a.T || a.slot[t] >= 0) return;
-  const int e = a.cand[(size_t)t * kMaxCand + a.r];
-  const int s = used_before(e) + a.hist[(size_t)(t / 32) * a.N + e] + a.local_rank[t];
-  if (s >= a.C) return;   // this candidate is full too
-  if (lane == 0) {
-    a.slot[t] = s;
-    a.drop[t] = 0;
-    a.expert_id[t] = e;
-    a.gate[t] = a.cand_p[(size_t)t * kMaxCand + a.r];
-    if (a.xbuf && a.tok_of_slot) a.tok_of_slot[(size_t)e * a.C + s] = t;
-  }
-  if (a.xbuf) {
-    const uint32_t rb = (uint32_t)a.d * (uint32_t)a.elem_bytes;
-    if (rb <= kStageRowMax) {
-      AssignArgs aa{};
-      aa.x = a.x; aa.xbuf = a.xbuf; aa.C = a.C; aa.status = a.status;
-      uint8_t* buf = rowbuf + (size_t)warp * rb;
-      stage_row_begin(aa, buf, &rowbar[warp], t, rb, lane);
-      stage_row_end(aa, buf, &rowbar[warp], e, s, rb, lane);
-    } else {
-      copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
-               static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kScanThreads) finish_kernel(ScanArgs a) {
+__global__ void __launch_bounds__(kExpandThreads, 1) expand_kernel(ExpandArgs a, ScanArgs fin) {
+  extern __shared__ int xsm[];
+  int* whist = xsm;                           // [kExpandWarps][N] group sizes
+  int* fill = xsm + kExpandWarps * a.N;       // [N] filled slots
   __shared__ int sh_i[33];
   __shared__ double sh_d[32];
   grid_dep_wait();
   grid_dep_launch();
-  finish_experts(a, sh_i, sh_d);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, N = a.N;
+  for (int i = tid; i < kExpandWarps * N; i += kExpandThreads) whist[i] = 0;
+  for (int e = tid; e < N; e += kExpandThreads) fill[e] = min(__ldcg(a.counts + e), a.C);
+  // tokens the top-1 pass left unplaced, in token order: each warp owns a
+  // contiguous run, read 32 tokens (one line) at a time, 8 lines in flight
+  const int perw = ((a.T + kExpandWarps * 32 - 1) / (kExpandWarps * 32)) * 32;
+  const int w0 = min(a.T, warp * perw), w1 = min(a.T, w0 + perw);
+  const unsigned lt = (1u << lane) - 1u;
+  int cw = 0;
+  for (int b = w0; b < w1; b += 8 * 32) {
+    int v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = b + j * 32 + lane;
+      v[j] = t < w1 ? __ldcg(a.slot + t) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cw += __popc(__ballot_sync(0xffffffffu, v[j] < 0));
+  }
+  int n;
+  int pos = __shfl_sync(0xffffffffu, block_exclusive_scan(lane == 0 ? cw : 0, &n, sh_i), 0);
+  for (int b = w0; b < w1; b += 8 * 32) {
+    int v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int t = b + j * 32 + lane;
+      v[j] = t < w1 ? __ldcg(a.slot + t) : 0;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const unsigned m = __ballot_sync(0xffffffffu, v[j] < 0);
+      if (v[j] < 0) a.open[pos + __popc(m & lt)] = b + j * 32 + lane;
+      pos += __popc(m);
+    }
+  }
+  int n_moved = 0;
+  __syncthreads();
+  for (int r = 1; r < a.k; ++r) {
+    int n_next = 0;
+    // the next chunk's tokens are loaded one chunk ahead: this chunk's
+    // compaction writes only positions below them
+    // (and their candidate and its probability once the token has arrived)
+    int t_nx = tid < n ? __ldcg(a.open + tid) : -1;
+    int e_nx = t_nx >= 0 ? __ldcg(a.cand + (size_t)t_nx * kMaxCand + r) : -1 - lane;
+    float g_nx = t_nx >= 0 ? __ldcg(a.cand_p + (size_t)t_nx * kMaxCand + r) : 0.f;
+    for (int c0 = 0; c0 < n; c0 += kExpandThreads) {
+      const int t = t_nx, e = e_nx;
+      const float gp = g_nx;
+      const int i_nx = c0 + kExpandThreads + tid;
+      t_nx = i_nx < n ? __ldcg(a.open + i_nx) : -1;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const bool leader = t >= 0 && (peers & lt) == 0;
+      if (leader) whist[warp * N + e] = __popc(peers);
+      __syncthreads();
+      int s = 0, pre = 0;
+      bool last = leader;
+      if (t >= 0) {
+        for (int w = 0; w < warp; ++w) pre += whist[w * N + e];
+        s = fill[e] + pre + __popc(peers & lt);
+        if (leader)
+          for (int w = warp + 1; w < kExpandWarps && last; ++w) last = whist[w * N + e] == 0;
+      }
+      __syncthreads();   // every read of whist and fill is done
+      e_nx = t_nx >= 0 ? __ldcg(a.cand + (size_t)t_nx * kMaxCand + r) : -1 - lane;
+      g_nx = t_nx >= 0 ? __ldcg(a.cand_p + (size_t)t_nx * kMaxCand + r) : 0.f;
+      if (leader) {
+        if (last) fill[e] += pre + __popc(peers);
+        whist[warp * N + e] = 0;
+      }
+      const bool placed = t >= 0 && s < a.C;
+      if (placed) {
+        a.slot[t] = s;
+        a.drop[t] = 0;
+        a.expert_id[t] = e;
+        a.gate[t] = gp;
+        if (a.tok_of_slot) a.tok_of_slot[(size_t)e * a.C + s] = t;
+      }
+      const bool stays = t >= 0 && !placed;
+      // one scan for both lists: stays in the low half, placed in the high
+      int tot;
+      const int p = block_exclusive_scan((int)stays | ((int)placed << 16), &tot, sh_i);
+      if (stays) a.open[n_next + (p & 0xffff)] = t;   // at or before position c0 + tid
+      if (placed) a.moved[n_moved + (p >> 16)] = t;
+      n_next += tot & 0xffff;
+      n_moved += tot >> 16;
+    }
+    n = n_next;
+    __syncthreads();
+    for (int e = tid; e < N; e += kExpandThreads) fill[e] = min(fill[e], a.C);
+    __syncthreads();
+  }
+  for (int e = tid; e < N; e += kExpandThreads) a.used[e] = fill[e];
+  if (tid == 0) *a.n_moved = n_moved;
+  __syncthreads();
+  finish_experts(fin, sh_i, sh_d);   // fin.kept == a.used
+}
+
+// Rows of the tokens passes 2..k placed, one warp per row.
+__global__ void __launch_bounds__(kRowWarps * 32) expand_dispatch_kernel(ExpandArgs a) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int lane = threadIdx.x & 31;
+  const int n = __ldcg(a.n_moved);
+  const uint32_t rb = (uint32_t)a.d * (uint32_t)a.elem_bytes;
+  for (int j = blockIdx.x * kRowWarps + (threadIdx.x >> 5); j < n; j += gridDim.x * kRowWarps) {
+    const int t = __ldcg(a.moved + j);
+    const int e = __ldcg(a.expert_id + t), s = __ldcg(a.slot + t);
+    copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
+             static_cast<char*>(a.xbuf) + ((size_t)e * a.C + s) * rb, (int)rb, lane);
+  }
 }
 
 constexpr int kSelThreads = 1024;
@@ -518,24 +585,17 @@ cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s, bool pdl) {
 
 namespace smoe {
 
-cudaError_t launch_expand_hist(const ExpandArgs& a, cudaStream_t s, bool pdl) {
-  const int groups = (a.T + 31) / 32;
-  return launch_k(expand_hist_kernel, dim3((groups + kRowWarps - 1) / kRowWarps),
-                  dim3(kRowWarps * 32), 0, s, pdl, a);
-}
-
-cudaError_t launch_expand_assign(const ExpandArgs& a, cudaStream_t s, bool pdl) {
-  const size_t rb = (size_t)a.d * a.elem_bytes;
-  const size_t smem = (a.xbuf && rb <= kStageRowMax) ? (size_t)kRowWarps * rb : 0;
-  cudaError_t err = cudaFuncSetAttribute(expand_assign_kernel,
+cudaError_t launch_expand(const ExpandArgs& a, const ScanArgs& fin, cudaStream_t s, bool pdl) {
+  const size_t smem = (size_t)(kExpandWarps + 1) * a.N * sizeof(int);
+  cudaError_t err = cudaFuncSetAttribute(expand_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_k(expand_assign_kernel, dim3((a.T + kRowWarps - 1) / kRowWarps + 1),
-                  dim3(kRowWarps * 32), smem, s, pdl, a);
+  return launch_k(expand_kernel, dim3(1), dim3(kExpandThreads), smem, s, pdl, a, fin);
 }
 
-cudaError_t launch_finish(const ScanArgs& a, cudaStream_t s, bool pdl) {
-  return launch_k(finish_kernel, dim3(1), dim3(kScanThreads), 0, s, pdl, a);
+cudaError_t launch_expand_dispatch(const ExpandArgs& a, cudaStream_t s, bool pdl) {
+  const int grid = std::min((a.T + kRowWarps - 1) / kRowWarps, 4 * 148);   // 4 per SM
+  return launch_k(expand_dispatch_kernel, dim3(grid), dim3(kRowWarps * 32), 0, s, pdl, a);
 }
 
 }  // namespace smoe

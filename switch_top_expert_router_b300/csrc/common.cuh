@@ -160,32 +160,28 @@ cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s, bool pdl = fals
 // ------------------------------------------- Expanded Drop, passes 2..k
 struct ExpandArgs {
   int T, N, C, d, elem_bytes;
-  int r;                       // candidate index of this pass (1..k-1)
+  int k;                       // candidates per token (2..kMaxCand)
   const int32_t* cand;         // [T][kMaxCand]
   const float* cand_p;         // [T][kMaxCand]
-  int32_t* hist;               // [R, N] this pass's group histograms (scanned in place)
-  int32_t* local_rank;         // [T]
-  const int32_t* pass_cnt;     // [N] this pass's per-expert totals (from the scan)
-  const int32_t* counts;       // [N] top-1 counts (first expand pass: used = min(counts, C))
-  const int32_t* used_in;      // [N] filled slots before this pass (null on the first)
-  int32_t* used_out;           // [N] filled slots after this pass
-  int32_t* expert_id;          // [T] updated for re-routed tokens
+  const int32_t* counts;       // [N] top-1 counts: pass 1 filled min(counts, C) slots
+  int32_t* open;               // [T] scratch: tokens still unplaced, in token order
+  int32_t* moved;              // [T] out: tokens placed by passes 2..k
+  int32_t* n_moved;            // [1] out: their number
+  int32_t* used;               // [N] out: filled slots after the last pass
+  int32_t* expert_id;          // [T] rewritten for moved tokens
   float* gate;
   int32_t* slot;
   uint8_t* drop;
+  int32_t* tok_of_slot;        // [N * C] or null
   const void* x;               // null: routing only
   void* xbuf;
-  int32_t* tok_of_slot;        // [N * C] or null
-  int* status;
 };
-// Per 32-token group: histogram and in-group ranks of the still-unplaced
-// tokens' r-th candidates.
-cudaError_t launch_expand_hist(const ExpandArgs& a, cudaStream_t s, bool pdl);
-// Place still-unplaced tokens on their r-th candidate when it has room;
-// one extra CTA writes used_out.
-cudaError_t launch_expand_assign(const ExpandArgs& a, cudaStream_t s, bool pdl);
-// finish_experts alone (one CTA), after the last Expanded Drop pass.
-cudaError_t launch_finish(const ScanArgs& a, cudaStream_t s, bool pdl);
+// Passes 2..k in one CTA, after the top-1 pass placed its tokens: the
+// unplaced tokens in token order try their next candidate while it has
+// room; then finish_experts over the final filled slots (fin.kept = used).
+cudaError_t launch_expand(const ExpandArgs& a, const ScanArgs& fin, cudaStream_t s, bool pdl);
+// Dispatch copies of the moved tokens' rows.
+cudaError_t launch_expand_dispatch(const ExpandArgs& a, cudaStream_t s, bool pdl);
 
 // ------------------------------------------------------- expert GEMMs
 // D[e, m, c] = sum_k A[e * M + m, k] * B[e * rows + nt * BN + c, k] for the
