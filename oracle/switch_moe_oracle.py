@@ -58,7 +58,8 @@ __all__ = [
     "TOKEN_ORDER", "GATE_PRIORITY",
     "capacity", "router_logits", "softmax", "top1", "route", "route_from_logits",
     "assign_slots", "expert_ffn", "aux_loss", "combine_token", "forward",
-    "forward_rows", "candidates", "assign_slots_expanded",
+    "forward_rows", "candidates", "assign_slots_expanded", "top2_gates",
+    "assign_slots_top2", "forward_top2",
 ]
 
 TOKEN_ORDER = 0
@@ -236,6 +237,56 @@ def assign_slots_expanded(cands, N: int, C: int):
 
 
 # --------------------------------------------------------------------------
+# Top-2 token choice, the variant the pages set beside Switch's top-1:
+#   [TOP1] industry-position and comparison sections (GShard, Mixtral:
+#   every token goes to 2 experts, is sent twice and needs a weighted
+#   merge); [SWITCH] Switch-layer section (Shazeer's top-k layer: logits
+#   h = W_r x, softmax-normalised gate values, the output is the gate-weighted
+#   sum over the chosen index set T); [CMP] routing table (Mixtral 8x7B:
+#   softmax over the top-k).
+# Readings, none of them printed on the pages:
+#   * the chosen set is the 2 highest logits, lowest index first on ties
+#     (candidates(logits, 2)); choice 0 is the top-1 expert;
+#   * capacity keeps the printed formula C = ceil(cf * T / N) (a caller who
+#     wants room for both choices passes a larger cf);
+#   * slots: first every token's choice 0 in token order (the top-1
+#     assignment), then every token's choice 1 in token order, after the
+#     choices the expert already kept; a (token, choice) pair is kept iff
+#     its slot < C;
+#   * gates: the chosen experts' softmax probabilities, or with renormalize
+#     the softmax over the two chosen logits, p_e / (p_e0 + p_e1);
+#   * y_t = sum over the token's kept choices of gate * E(x_t); a dropped
+#     choice adds nothing and the other gate is not re-scaled;
+#   * expert_counts (f_i of L_aux) count choice 0, the router's top-1.
+# --------------------------------------------------------------------------
+def top2_gates(probs, cands, renormalize: int) -> np.ndarray:
+    """float64 [T, 2]: the gate of each chosen expert."""
+    p = _f64(probs)
+    cands = np.asarray(cands, dtype=np.int64)
+    rows = np.arange(p.shape[0])
+    g = np.stack([p[rows, cands[:, 0]], p[rows, cands[:, 1]]], axis=1)
+    if renormalize:
+        g = g / g.sum(axis=1, keepdims=True)
+    return g
+
+
+def assign_slots_top2(cands, N: int, C: int):
+    """Returns (slot int64[T, 2] with -1 for a dropped choice, drop uint8[T, 2],
+    used int64[N] = filled slots per expert)."""
+    cands = np.asarray(cands, dtype=np.int64)
+    T = cands.shape[0]
+    used = np.zeros(N, dtype=np.int64)
+    slot = np.full((T, 2), -1, dtype=np.int64)
+    for r in range(2):                        # all first choices, then all second
+        for t in range(T):                    # token order
+            e = cands[t, r]
+            if used[e] < C:
+                slot[t, r] = used[e]
+                used[e] += 1
+    return slot, (slot < 0).astype(np.uint8), used
+
+
+# --------------------------------------------------------------------------
 # Step a6/a7: the expert, a two-layer bias-free FFN ([TOP1] key-parameter
 # section: about 2 * d_model * d_ff weights per expert).  ReLU between.
 #   W1_e: [d_ff, d_model], W2_e: [d_model, d_ff] (out-features first).
@@ -311,6 +362,45 @@ def forward(x, W_g, W1, W2, capacity_factor: float, priority_mode: int = TOKEN_O
                              None if S is None else S[t])
     return {"y": y, "expert_id": expert_id, "gate": gate, "slot": slot,
             "drop": drop, "counts": counts, "aux_loss": aux_loss(r["probs"], counts),
+            "logits": r["logits"], "probs": r["probs"], "capacity": C}
+
+
+def forward_top2(x, W_g, W1, W2, capacity_factor: float, gate_multiply: int = 1,
+                 renormalize: int = 0, b_g=None, W1s=None, W2s=None,
+                 expert_getter: Optional[Callable[[int], tuple]] = None):
+    """The layer with top-2 routing (token order).  Returns a dict with y
+    (fp64 [T, d]), expert_id / gate / slot / drop as [T, 2] (choice 0 =
+    the top-1 expert), counts of choice 0 and aux_loss."""
+    r = route(x, W_g, b_g)
+    T, N = r["probs"].shape
+    if N < 2:
+        raise ValueError("top-2 routing needs at least two experts")
+    C = capacity(T, N, capacity_factor)
+    cands = candidates(r["logits"], 2)
+    gate = top2_gates(r["probs"], cands, renormalize)
+    slot, drop, _ = assign_slots_top2(cands, N, C)
+    counts = np.bincount(cands[:, 0], minlength=N).astype(np.int64)
+    d = x.shape[1]
+    o = np.zeros((T, 2, d), dtype=np.float64)
+    for i in range(N):
+        sel = [(t, c) for c in range(2) for t in np.nonzero((cands[:, c] == i) & (slot[:, c] >= 0))[0]]
+        if not sel:
+            continue
+        W1_e, W2_e = expert_getter(i) if expert_getter else (W1[i], W2[i])
+        ts = np.array([t for t, _ in sel])
+        out = expert_ffn(_rows(x, ts), W1_e, W2_e)
+        for k, (t, c) in enumerate(sel):
+            o[t, c] = out[k]
+    S = expert_ffn(x, W1s, W2s) if W1s is not None else None
+    y = np.zeros((T, d), dtype=np.float64)
+    for t in range(T):
+        acc = np.zeros(d, dtype=np.float64)
+        for c in range(2):                     # the weighted merge of the kept choices
+            if not drop[t, c]:
+                acc = acc + (gate[t, c] if gate_multiply else 1.0) * o[t, c]
+        y[t] = acc if S is None else acc + S[t]
+    return {"y": y, "expert_id": cands, "gate": gate, "slot": slot, "drop": drop,
+            "counts": counts, "aux_loss": aux_loss(r["probs"], counts),
             "logits": r["logits"], "probs": r["probs"], "capacity": C}
 
 

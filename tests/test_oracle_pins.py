@@ -515,3 +515,148 @@ def test_forward_expanded_reroutes_with_candidate_gate():
                            rtol=1e-12, atol=1e-12)
     same = np.nonzero(base["drop"] == 0)[0]                  # pass-1 tokens are untouched
     assert np.array_equal(ex["y"][same], base["y"][same])
+
+
+# ------------------------------------------------------------------ Top-2
+def _golden_top2():
+    slots, gates, cands, N = [], [], None, 0
+    for line in open(os.path.join(GOLDEN, "top2.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        if line.startswith("chosen"):
+            f = line.split()
+            N = int(f[1].split("=")[1])
+            cands = np.array([[int(v) for v in c.split(",")] for c in f[2:]])
+        elif line.startswith("gates"):
+            lg, ch, g, gr = (part.split() for part in line[len("gates"):].split("|"))
+            logits = [math.log(float(v[2:])) if v.startswith("ln") else float(v)
+                      for v in lg[0].split(",")]
+            gates.append((np.array([logits]), [int(v) for v in ch], [float(v) for v in g],
+                          [float(v) for v in gr]))
+        else:
+            c, s0, s1, u = (part.split() for part in line.split("|"))
+            slots.append((cands, N, int(c[0]), [int(v) for v in s0], [int(v) for v in s1],
+                          [int(v) for v in u]))
+    return slots, gates
+
+
+@pytest.mark.parametrize("case", _golden_top2()[0], ids=lambda c: f"C{c[2]}")
+def test_top2_slots_golden(case):
+    cands, N, C, want0, want1, want_u = case
+    slot, drop, used = O.assign_slots_top2(cands, N, C)
+    assert slot[:, 0].tolist() == want0 and slot[:, 1].tolist() == want1
+    assert used.tolist() == want_u
+    assert np.array_equal(drop, (slot < 0).astype(np.uint8))
+
+
+@pytest.mark.parametrize("case", _golden_top2()[1], ids=lambda c: str(c[1]))
+def test_top2_gates_golden(case):
+    logits, chosen, g, gr = case
+    c = O.candidates(logits, 2)
+    assert c[0].tolist() == chosen
+    p = O.softmax(logits)
+    np.testing.assert_allclose(O.top2_gates(p, c, 0)[0], g, rtol=1e-15)
+    np.testing.assert_allclose(O.top2_gates(p, c, 1)[0], gr, rtol=1e-15)
+
+
+def test_top2_first_choices_are_the_top1_assignment():
+    rng = np.random.default_rng(11)
+    for T, N, C in [(300, 5, 40), (64, 8, 3), (500, 16, 20)]:
+        l = rng.normal(size=(T, N)) + np.linspace(0, 1.5, N)
+        c = O.candidates(l, 2)
+        slot, _, _ = O.assign_slots_top2(c, N, C)
+        s0, _, counts = O.assign_slots(c[:, 0], np.ones(T), N, C, O.TOKEN_ORDER)
+        assert np.array_equal(slot[:, 0], s0)
+        # every second choice an expert keeps sits after all of its kept first choices
+        for i in range(N):
+            second = slot[(c[:, 1] == i) & (slot[:, 1] >= 0), 1]
+            assert np.all(second >= min(counts[i], C))
+
+
+def test_top2_invariants():
+    rng = np.random.default_rng(12)
+    for T, N, C in [(400, 6, 50), (128, 4, 20), (1000, 16, 40), (37, 3, 1), (50, 2, 60)]:
+        l = rng.normal(size=(T, N)) + np.linspace(0, 2, N)
+        c = O.candidates(l, 2)
+        assert np.all(c[:, 0] != c[:, 1])
+        slot, drop, used = O.assign_slots_top2(c, N, C)
+        assert np.all(used <= C)
+        for i in range(N):   # both choices together fill slots 0 .. used - 1 once each
+            s = np.concatenate([slot[(c[:, r] == i) & (slot[:, r] >= 0), r] for r in range(2)])
+            assert sorted(s.tolist()) == list(range(used[i]))
+            for r in range(2):   # token order within a pass
+                sr = slot[(c[:, r] == i) & (slot[:, r] >= 0), r]
+                assert np.all(np.diff(sr) > 0)
+        if 2 * T <= C:
+            assert drop.sum() == 0
+        p = O.softmax(l)
+        g = O.top2_gates(p, c, 0)
+        assert np.all(g[:, 0] >= g[:, 1]) and np.all(g.sum(axis=1) <= 1 + 1e-15)
+        np.testing.assert_allclose(O.top2_gates(p, c, 1).sum(axis=1), 1.0, rtol=1e-15)
+
+
+def test_top2_brute_force_definition():
+    """Kept iff fewer than C earlier (pass-major, then token order) choices
+    hold the same expert: the O(T^2) definition, over every assignment of
+    ordered expert pairs for small T."""
+    N = 3
+    pairs = [(a, b) for a in range(N) for b in range(N) if a != b]
+    rng = np.random.default_rng(13)
+    for T in (1, 2, 3, 4):
+        combos = list(itertools.product(pairs, repeat=T))
+        if len(combos) > 400:
+            combos = [combos[i] for i in rng.choice(len(combos), 400, replace=False)]
+        for combo in combos:
+            c = np.array(combo)
+            order = [(r, t) for r in range(2) for t in range(T)]
+            for C in range(1, 2 * T + 1):
+                slot, _, _ = O.assign_slots_top2(c, N, C)
+                for k, (r, t) in enumerate(order):
+                    before = sum(1 for (r2, t2) in order[:k] if c[t2, r2] == c[t, r])
+                    # slot = number of earlier choices the expert kept
+                    want = before if before < C else -1
+                    assert slot[t, r] == want
+
+
+def test_forward_top2_identical_experts_closed_form():
+    """All experts equal, nothing dropped: y = (g0 + g1) E(x); with
+    renormalised gates that is E(x) itself (checked against torch float64)."""
+    rng = np.random.default_rng(14)
+    T, d, F, N = 40, 12, 20, 5
+    x = torch.tensor(rng.normal(size=(T, d)))
+    W_g = torch.tensor(rng.normal(size=(N, d)))
+    w1 = torch.tensor(rng.normal(size=(F, d)) / np.sqrt(d))
+    w2 = torch.tensor(rng.normal(size=(d, F)) / np.sqrt(F))
+    W1, W2 = w1.expand(N, F, d).clone(), w2.expand(N, d, F).clone()
+    E = torch.nn.functional.linear(torch.relu(torch.nn.functional.linear(x, w1)), w2).numpy()
+    cf = float(2 * N)   # C >= 2T: both choices of every token fit
+    out = O.forward_top2(x, W_g, W1, W2, cf, gate_multiply=1, renormalize=1)
+    assert out["drop"].sum() == 0
+    np.testing.assert_allclose(out["y"], E, rtol=1e-12, atol=1e-12)
+    out = O.forward_top2(x, W_g, W1, W2, cf, gate_multiply=1, renormalize=0)
+    p = torch.softmax(x @ W_g.T, dim=1).numpy()
+    top2 = np.sort(p, axis=1)[:, -2:].sum(axis=1)
+    np.testing.assert_allclose(out["y"], top2[:, None] * E, rtol=1e-12, atol=1e-12)
+    out = O.forward_top2(x, W_g, W1, W2, cf, gate_multiply=0)
+    np.testing.assert_allclose(out["y"], 2 * E, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_top2_zero_second_expert_is_top1():
+    """N = 2 with expert 0 always first: choice 1 is expert 1; with W of
+    expert 1 zero the layer is the top-1 layer with the same gate."""
+    rng = np.random.default_rng(15)
+    T, d, F = 30, 8, 16
+    x = torch.tensor(rng.normal(size=(T, d)))
+    W_g = torch.tensor(rng.normal(size=(2, d)) * 0.1)
+    b_g = torch.tensor([5.0, 0.0])
+    W1 = torch.tensor(rng.normal(size=(2, F, d)))
+    W2 = torch.tensor(rng.normal(size=(2, d, F)))
+    W1[1] = 0
+    for cf in (0.5, 2.0):
+        a = O.forward_top2(x, W_g, W1, W2, cf, gate_multiply=1, b_g=b_g)
+        b = O.forward(x, W_g, W1, W2, cf, gate_multiply=1, b_g=b_g)
+        assert np.all(a["expert_id"][:, 0] == 0)
+        np.testing.assert_allclose(a["y"], b["y"], rtol=1e-13, atol=1e-13)
+        assert np.array_equal(a["slot"][:, 0], b["slot"])
+        assert a["aux_loss"] == b["aux_loss"]
