@@ -107,6 +107,30 @@ typedef struct switch_moe_params {
    * expert_counts and aux_loss keep the router's top-1 choices.  Token-order
    * priority only (SWITCH_MOE_ERR_UNSUPPORTED otherwise); k <= N. */
   int32_t expand;
+  /* Experts per token: 0 or 1 = top-1 (Switch); 2 = top-2 token choice
+   * ([TOP1] industry-position and comparison sections: GShard and Mixtral
+   * send every token to two experts and merge the outputs with weights;
+   * [SWITCH] Switch-layer section: the top-k layer's output is the
+   * gate-weighted sum over the chosen set).  The chosen pair is the two
+   * highest logits, lowest index first on ties; choice 0 is the top-1
+   * expert.  Capacity is the same C = ceil(cf * T / N) (pass a larger cf to
+   * make room for both choices).  Slots: every token's choice 0 in token
+   * order first (the top-1 assignment), then every token's choice 1 in
+   * token order after the slots its expert already holds; a choice is kept
+   * iff its slot < C.  y[t] = sum over the kept choices of g * E(x_t) (+ the
+   * shared expert); a dropped choice adds nothing.  With top_k == 2 the
+   * per-token outputs expert_id, gate, slot and drop_mask are [T, 2]
+   * (row-major, choice fastest); expert_counts and aux_loss count choice 0
+   * (the router's top-1).  Token-order priority, N >= 2 and expand <= 1
+   * only (SWITCH_MOE_ERR_UNSUPPORTED otherwise).  The two adds into a y row
+   * are atomic: with a shared expert (three terms) their order, and so the
+   * last bit of y, can differ between runs. */
+  int32_t top_k;
+  /* top_k == 2 only (SWITCH_MOE_ERR_INVALID_ARG otherwise): 0 = the gates are
+   * the chosen experts' softmax probabilities over all N; 1 = softmax over
+   * the two chosen logits, p_e / (p_e0 + p_e1) ([CMP] routing table,
+   * Mixtral: softmax over the top-k). */
+  int32_t renormalize;
 } switch_moe_params;
 
 /* Expert capacity C = ceil(cf * T / N), evaluated in double as (cf*T)/N.

@@ -59,7 +59,7 @@ __all__ = [
     "capacity", "router_logits", "softmax", "top1", "route", "route_from_logits",
     "assign_slots", "expert_ffn", "aux_loss", "combine_token", "forward",
     "forward_rows", "candidates", "assign_slots_expanded", "top2_gates",
-    "assign_slots_top2", "forward_top2",
+    "assign_slots_top2", "forward_top2", "forward_rows_top2",
 ]
 
 TOKEN_ORDER = 0
@@ -425,6 +425,17 @@ def forward_rows(rows: Sequence[int], x, expert_id, gate, slot, gate_multiply: i
         out[k] = combine_token(o[k], g[k], bool(s[k] < 0), bool(gate_multiply), d,
                                None if S is None else S[k])
     return out
+
+
+def forward_rows_top2(rows: Sequence[int], x, expert_id, gate, slot, gate_multiply: int,
+                      expert_getter: Callable[[int], tuple], W1s=None, W2s=None) -> np.ndarray:
+    """forward_rows under top-2 routing decisions (expert_id, gate, slot as
+    [T, 2]): the sum of the two choices' rows, the shared expert once."""
+    e, g, s = (np.asarray(a) for a in (expert_id, gate, slot))
+    first = forward_rows(rows, x, e[:, 0], g[:, 0], s[:, 0], gate_multiply, expert_getter,
+                         W1s, W2s)
+    second = forward_rows(rows, x, e[:, 1], g[:, 1], s[:, 1], gate_multiply, expert_getter)
+    return first + second
 
 
 def _rows(x, rows):

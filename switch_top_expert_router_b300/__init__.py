@@ -62,7 +62,8 @@ class Params(ctypes.Structure):
         ("N", ctypes.c_int64), ("capacity_factor", ctypes.c_double),
         ("priority_mode", ctypes.c_int32), ("gate_multiply", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("has_shared", ctypes.c_int32),
-        ("expand", ctypes.c_int32),
+        ("expand", ctypes.c_int32), ("top_k", ctypes.c_int32),
+        ("renormalize", ctypes.c_int32),
     ]
 
 
@@ -181,10 +182,24 @@ def switch_moe_capacity(T: int, N: int, capacity_factor: float) -> int:
 
 
 def make_params(T, d_model, d_ff, N, capacity_factor, priority_mode=TOKEN_ORDER,
-                gate_multiply=1, dtype=BF16, has_shared=0, expand=1) -> Params:
+                gate_multiply=1, dtype=BF16, has_shared=0, expand=1, top_k=1,
+                renormalize=0) -> Params:
     return Params(int(T), int(d_model), int(d_ff), int(N), float(capacity_factor),
                   int(priority_mode), int(gate_multiply), int(dtype), int(has_shared),
-                  int(expand))
+                  int(expand), int(top_k), int(renormalize))
+
+
+def _token_shape(T: int, top_k: int) -> tuple:
+    """Shape of the per-token routing outputs: [T], or [T, 2] for top-2."""
+    return (T, 2) if top_k == 2 else (T,)
+
+
+def _check_out(out, T: int, d: int, N: int, top_k: int, names) -> None:
+    """Output tensors the caller passed must have the sizes the library writes."""
+    want = [T * d] + [T * (2 if top_k == 2 else 1)] * (len(names) - 3) + [N, 1]
+    for t, n, name in zip(out, want, names):
+        if t.numel() != n or not t.is_contiguous():
+            raise ValueError(f"out.{name} must be contiguous with {n} elements")
 
 
 def switch_moe_workspace_bytes(p: Params) -> int:
@@ -252,27 +267,31 @@ def switch_moe_forward(x: torch.Tensor, W_g: torch.Tensor, W1: torch.Tensor, W2:
                        gate_multiply: int = 1, b_g: Optional[torch.Tensor] = None,
                        W1s: Optional[torch.Tensor] = None, W2s: Optional[torch.Tensor] = None,
                        ws: Optional[torch.Tensor] = None, out: Optional[ForwardOut] = None,
-                       stream=None, expand: int = 1) -> ForwardOut:
+                       stream=None, expand: int = 1, top_k: int = 1,
+                       renormalize: int = 0) -> ForwardOut:
     """The whole layer; see switch_moe_forward in include/switch_moe.h
-    (expand: Expanded Drop candidates, 1 = off)."""
+    (expand: Expanded Drop candidates, 1 = off; top_k: 1 or 2 experts per
+    token, renormalize: top-2 gates over the chosen pair)."""
     if not x.is_cuda:
         raise ValueError("x must be a CUDA tensor (use switch_moe_forward_hostio for host data)")
     dev = x.device
     _contig(x, "x", None, dev)
     T, d, F, N = _layer_args(x, W_g, W1, W2, b_g, W1s, W2s, dev)
     p = make_params(T, d, F, N, capacity_factor, priority_mode, gate_multiply, _dtype_code(x),
-                    int(W1s is not None), expand)
+                    int(W1s is not None), expand, top_k, renormalize)
     need = switch_moe_workspace_bytes(p)
     if ws is None:
         ws = workspace(need, dev)
+    ts = _token_shape(T, top_k)
     if out is None:
         out = ForwardOut(torch.empty((T, d), dtype=torch.float32, device=dev),
-                         torch.empty(T, dtype=torch.int32, device=dev),
-                         torch.empty(T, dtype=torch.float32, device=dev),
-                         torch.empty(T, dtype=torch.int32, device=dev),
-                         torch.empty(T, dtype=torch.uint8, device=dev),
+                         torch.empty(ts, dtype=torch.int32, device=dev),
+                         torch.empty(ts, dtype=torch.float32, device=dev),
+                         torch.empty(ts, dtype=torch.int32, device=dev),
+                         torch.empty(ts, dtype=torch.uint8, device=dev),
                          torch.empty(N, dtype=torch.int32, device=dev),
                          torch.empty(1, dtype=torch.float32, device=dev))
+    _check_out(out, T, d, N, top_k, ForwardOut._fields)
     with torch.cuda.device(dev):
         rc = _lib.switch_moe_forward(
             ctypes.byref(p), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(W1), _ptr(W2), _ptr(W1s),
@@ -291,7 +310,8 @@ def switch_moe_forward_hostio(x_host: torch.Tensor, W_g: torch.Tensor, W1: torch
                               W2s: Optional[torch.Tensor] = None,
                               ws: Optional[torch.Tensor] = None,
                               out: Optional[ForwardOut] = None, stream=None,
-                              expand: int = 1) -> ForwardOut:
+                              expand: int = 1, top_k: int = 1,
+                              renormalize: int = 0) -> ForwardOut:
     """Host input and output tensors (pin them for asynchronous copies);
     device weights.  Outputs are valid after the stream is synchronised."""
     if x_host.is_cuda:
@@ -300,19 +320,21 @@ def switch_moe_forward_hostio(x_host: torch.Tensor, W_g: torch.Tensor, W1: torch
     _contig(x_host, "x_host")
     T, d, F, N = _layer_args(x_host, W_g, W1, W2, b_g, W1s, W2s, dev)
     p = make_params(T, d, F, N, capacity_factor, priority_mode, gate_multiply,
-                    _dtype_code(x_host), int(W1s is not None), expand)
+                    _dtype_code(x_host), int(W1s is not None), expand, top_k, renormalize)
     need = switch_moe_hostio_workspace_bytes(p)
     if ws is None:
         ws = workspace(need, dev)
+    ts = _token_shape(T, top_k)
     if out is None:
         pin = torch.cuda.is_available()
         out = ForwardOut(torch.empty((T, d), dtype=torch.float32, pin_memory=pin),
-                         torch.empty(T, dtype=torch.int32, pin_memory=pin),
-                         torch.empty(T, dtype=torch.float32, pin_memory=pin),
-                         torch.empty(T, dtype=torch.int32, pin_memory=pin),
-                         torch.empty(T, dtype=torch.uint8, pin_memory=pin),
+                         torch.empty(ts, dtype=torch.int32, pin_memory=pin),
+                         torch.empty(ts, dtype=torch.float32, pin_memory=pin),
+                         torch.empty(ts, dtype=torch.int32, pin_memory=pin),
+                         torch.empty(ts, dtype=torch.uint8, pin_memory=pin),
                          torch.empty(N, dtype=torch.int32, pin_memory=pin),
                          torch.empty(1, dtype=torch.float32, pin_memory=pin))
+    _check_out(out, T, d, N, top_k, ForwardOut._fields)
     with torch.cuda.device(dev):
         rc = _lib.switch_moe_forward_hostio(
             ctypes.byref(p), _ptr(x_host), _ptr(W_g), _ptr(b_g), _ptr(W1), _ptr(W2),
@@ -326,19 +348,23 @@ def switch_moe_forward_hostio(x_host: torch.Tensor, W_g: torch.Tensor, W1: torch
 def switch_moe_route_from_logits(logits: torch.Tensor, capacity_factor: float,
                                  priority_mode: int = TOKEN_ORDER,
                                  ws: Optional[torch.Tensor] = None,
-                                 stream=None, expand: int = 1) -> RouteOut:
-    """Routing on given fp32 logits [T, N] (expand: Expanded Drop candidates)."""
+                                 stream=None, expand: int = 1, top_k: int = 1,
+                                 renormalize: int = 0) -> RouteOut:
+    """Routing on given fp32 logits [T, N] (expand: Expanded Drop candidates;
+    top_k: 1 or 2 experts per token; renormalize: top-2 gates over the pair)."""
     dev = logits.device
     _contig(logits, "logits", torch.float32)
     T, N = logits.shape
-    p = make_params(T, 8, 8, N, capacity_factor, priority_mode, 1, F32, 0, expand)
+    p = make_params(T, 8, 8, N, capacity_factor, priority_mode, 1, F32, 0, expand, top_k,
+                    renormalize)
     need = switch_moe_workspace_bytes(p)
     if ws is None:
         ws = workspace(need, dev)
-    o = RouteOut(torch.empty(T, dtype=torch.int32, device=dev),
-                 torch.empty(T, dtype=torch.float32, device=dev),
-                 torch.empty(T, dtype=torch.int32, device=dev),
-                 torch.empty(T, dtype=torch.uint8, device=dev),
+    ts = _token_shape(T, top_k)
+    o = RouteOut(torch.empty(ts, dtype=torch.int32, device=dev),
+                 torch.empty(ts, dtype=torch.float32, device=dev),
+                 torch.empty(ts, dtype=torch.int32, device=dev),
+                 torch.empty(ts, dtype=torch.uint8, device=dev),
                  torch.empty(N, dtype=torch.int32, device=dev),
                  torch.empty(1, dtype=torch.float32, device=dev))
     with torch.cuda.device(dev):

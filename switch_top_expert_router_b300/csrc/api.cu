@@ -96,6 +96,8 @@ struct Plan {
   bool bf16;
   int mode, gm, shared;
   int expand;        // Expanded Drop candidates (1 = plain top-1)
+  int topk;          // experts per token: 1, or 2 (top-2 token choice)
+  int renorm;        // top-2 gates renormalised over the pair
   int elem;          // bytes per x/W element
   int BN, BNs;       // token tiles: routed experts, shared expert
   int max_entries;   // N * ceil(C / BN)
@@ -105,7 +107,8 @@ struct Plan {
   int part_units;    // tail-split partial tiles of the tensor-core GEMMs
   // workspace offsets
   bool tc_router;    // bf16 x and N <= kMaxExpertsTc: tensor-core router
-  size_t o_cand, o_candp, o_used;   // Expanded Drop
+  size_t o_cand, o_candp, o_used;   // Expanded Drop and top-2
+  size_t o_hist2, o_rank2, o_cnt2, o_e1, o_g1;   // top-2
   size_t o_Ppart, o_hist, o_rank, o_Psum, o_start, o_list, o_entries, o_ctrl, o_wsplit, o_xbuf,
       o_H0, o_H1, o_O, o_Hs0, o_Hs1, o_Os, o_tok, o_part, o_splitcnt, total;
   // extra for the host-IO entry point
@@ -142,6 +145,11 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   if (p->N > kMaxExperts) return SWITCH_MOE_ERR_UNSUPPORTED;
   if (p->expand > 1 && (p->priority_mode != SWITCH_MOE_TOKEN_ORDER || p->expand > p->N))
     return SWITCH_MOE_ERR_UNSUPPORTED;
+  if (p->top_k < 0 || p->top_k > 2 || (p->renormalize != 0 && p->renormalize != 1))
+    return SWITCH_MOE_ERR_INVALID_ARG;
+  if (p->renormalize && p->top_k != 2) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (p->top_k == 2 && (p->priority_mode != SWITCH_MOE_TOKEN_ORDER || p->expand > 1 || p->N < 2))
+    return SWITCH_MOE_ERR_UNSUPPORTED;
   if (need_gemm && (p->d_model < 8 || p->d_ff < 8 || p->d_model % 8 || p->d_ff % 8))
     return SWITCH_MOE_ERR_UNSUPPORTED;
   if (p->T > (int64_t)1 << 30 || p->d_model > (1 << 20) || p->d_ff > (1 << 20))
@@ -153,6 +161,8 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   q.elem = q.bf16 ? 2 : 4;
   q.mode = p->priority_mode; q.gm = p->gate_multiply; q.shared = p->has_shared;
   q.expand = p->expand > 1 ? p->expand : 1;
+  q.topk = p->top_k == 2 ? 2 : 1;
+  q.renorm = p->renormalize;
   if (q.T == 0) return SWITCH_MOE_OK;
   const int64_t C = capacity_of(q.T, q.N, p->capacity_factor);
   if (C < 1) return SWITCH_MOE_ERR_INVALID_ARG;
@@ -185,10 +195,17 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   q.o_list = take((size_t)q.T * 4);
   q.o_entries = take((size_t)q.max_entries * 8);
   q.o_ctrl = take(64);
-  if (q.expand > 1) {
+  if (q.expand > 1 || q.topk == 2) {
     q.o_cand = take((size_t)q.T * kMaxCand * 4);
     q.o_candp = take((size_t)q.T * kMaxCand * 4);
-    q.o_used = take((size_t)q.N * 4);   // filled slots after the last pass
+    q.o_used = take((size_t)q.N * 4);   // filled slots after the last pass / both choices
+  }
+  if (q.topk == 2) {
+    q.o_hist2 = take((size_t)q.R * q.N * 4);
+    q.o_rank2 = take((size_t)q.T * 4);
+    q.o_cnt2 = take((size_t)q.N * 4);
+    q.o_e1 = take((size_t)q.T * 4);   // the router's top-1 outputs (the user's are [T, 2])
+    q.o_g1 = take((size_t)q.T * 4);
   }
   q.tc_router = q.bf16 && q.N <= kMaxExpertsTc;
   if (q.tc_router) q.o_wsplit = take((size_t)3 * router_tc_n_mma((int)q.N) * q.d * 2);
@@ -227,10 +244,10 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   q.total = o;
   q.o_xin = take((size_t)q.T * q.d * q.elem);
   q.o_y = take((size_t)q.T * q.d * 4);
-  q.o_eid = take((size_t)q.T * 4);
-  q.o_gate = take((size_t)q.T * 4);
-  q.o_slot = take((size_t)q.T * 4);
-  q.o_drop = take((size_t)q.T);
+  q.o_eid = take((size_t)q.T * q.topk * 4);
+  q.o_gate = take((size_t)q.T * q.topk * 4);
+  q.o_slot = take((size_t)q.T * q.topk * 4);
+  q.o_drop = take((size_t)q.T * q.topk);
   q.o_cnt = take((size_t)q.N * 4);
   q.o_aux = take(4);
   q.total_hostio = o;
@@ -280,10 +297,18 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   ra.expert_id = expert_id; ra.gate = gate;
   ra.P_part = at<float>(ws, q.o_Ppart); ra.hist = at<int32_t>(ws, q.o_hist);
   ra.local_rank = at<int32_t>(ws, q.o_rank); ra.ctrl = ctrl;
-  ra.n_cand = q.expand;
-  if (q.expand > 1) {
+  ra.n_cand = q.expand > q.topk ? q.expand : q.topk;
+  if (ra.n_cand > 1) {
     ra.cand = at<int32_t>(ws, q.o_cand);
     ra.cand_p = at<float>(ws, q.o_candp);
+  }
+  if (q.topk == 2) {
+    // the router's top-1 expert and gate go to scratch; the slot step
+    // writes the [T, 2] outputs from the two candidates
+    ra.expert_id = at<int32_t>(ws, q.o_e1);
+    ra.gate = at<float>(ws, q.o_g1);
+    ra.hist2 = at<int32_t>(ws, q.o_hist2);
+    ra.local_rank2 = at<int32_t>(ws, q.o_rank2);
   }
   mark(0, s);
   if (x && q.tc_router) {
@@ -306,6 +331,11 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
     sa.split_cnt = at<int32_t>(ws, q.o_splitcnt);
     sa.n_split_cnt = 4 * q.part_units + q.max_entries + 1;
   }
+  if (q.topk == 2) {
+    sa.hist2 = ra.hist2;
+    sa.counts2 = at<int32_t>(ws, q.o_cnt2);
+    sa.kept_out = at<int32_t>(ws, q.o_used);
+  }
   if (launch_scan(sa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   mark(2, s);
 
@@ -318,6 +348,12 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
   aa.tok_of_slot = (dispatch && q.fused) ? at<int32_t>(ws, q.o_tok) : nullptr;
   aa.y = (dispatch && q.fused && !q.shared) ? y : nullptr;
   aa.status = status;
+  if (q.topk == 2) {
+    aa.topk = 2; aa.renorm = q.renorm;
+    aa.cand = ra.cand; aa.cand_p = ra.cand_p;
+    aa.bases2 = ra.hist2; aa.local_rank2 = ra.local_rank2;
+    aa.eid_out = expert_id; aa.gate_out = gate;
+  }
   // with Expanded Drop the work list waits for the last pass (launch_expand)
   const bool finish_here = sa.defer_finish && q.expand == 1;
   if (launch_assign(aa, finish_here ? &sa : nullptr, s, true) != cudaSuccess)
@@ -371,7 +407,10 @@ int run_gemm(const Plan& q, const DeviceInfo* dev, bool dense, int layer, const 
     g.tok_of_slot = at<int32_t>(ws, q.o_tok);
     g.gate = gate;
     g.gate_multiply = q.gm;
-    g.y_acc = q.shared;   // the shared expert's output is already in y
+    g.tok_shift = q.topk - 1;
+    // top-2: two choices add into a row (zeroed, or holding the shared
+    // expert's output); top-1: the shared expert's output is already in y
+    g.y_acc = q.topk == 2 ? 2 : q.shared;
   }
   if (!dense && q.part_units) {
     g.part = at<float>(ws, q.o_part);
@@ -443,7 +482,8 @@ int run_ffn(const Plan& q, const DeviceInfo* dev, const void* W1, const void* W2
   a.n_experts = (int)q.N;
   a.H0 = at<__nv_bfloat16>(ws, q.o_H0); a.H1 = at<__nv_bfloat16>(ws, q.o_H1);
   a.y = y; a.tok_of_slot = at<int32_t>(ws, q.o_tok); a.gate = gate;
-  a.gate_multiply = q.gm; a.y_acc = q.shared;
+  a.gate_multiply = q.gm; a.tok_shift = q.topk - 1;
+  a.y_acc = q.topk == 2 ? 2 : q.shared;
   a.part = at<float>(ws, q.o_part); a.part_units = q.part_units;
   a.split_cnt = at<int32_t>(ws, q.o_splitcnt);
   a.stages = ffn_tc_stages(q.BN);
@@ -468,8 +508,9 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
   int rc = run_routing(q, x, W_g, b_g, nullptr, expert_id, gate, slot, drop, counts, aux, ws,
                        true, y, dev->status, s);
   if (rc) return rc;
-  // filled slots per expert: min(counts, C), or after Expanded Drop its passes' total
-  const int32_t* kept = q.expand > 1 ? at<int32_t>(ws, q.o_used) : counts;
+  // filled slots per expert: min(counts, C), or after Expanded Drop its
+  // passes' total, or with top-2 both choices' total
+  const int32_t* kept = (q.expand > 1 || q.topk == 2) ? at<int32_t>(ws, q.o_used) : counts;
   void* xbuf = at<void>(ws, q.o_xbuf);
   void* H0 = at<void>(ws, q.o_H0);
   void* H1 = q.bf16 ? at<void>(ws, q.o_H1) : nullptr;
@@ -510,7 +551,8 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
   CombineArgs ca{};
   ca.T = (int)q.T; ca.d = (int)q.d; ca.C = q.C;
   ca.ksplit = q.bf16 ? q.ksplit : 1;
-  ca.gate_multiply = q.gm; ca.expert_id = expert_id; ca.gate = gate; ca.slot = slot;
+  ca.gate_multiply = q.gm; ca.topk = q.topk;
+  ca.expert_id = expert_id; ca.gate = gate; ca.slot = slot;
   ca.O = O; ca.split_stride = (size_t)q.N * q.C * q.d; ca.S = Os; ca.y = y;
   if (launch_combine(ca, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   mark(7, s);
@@ -620,16 +662,16 @@ int switch_moe_forward_hostio(const switch_moe_params* p, const void* x_host, co
                         at<int32_t>(workspace, q.o_slot), at<uint8_t>(workspace, q.o_drop), d_cnt,
                         d_aux, workspace, s);
     if (rc) return rc;
-    const size_t T = (size_t)q.T;
+    const size_t T = (size_t)q.T, Tk = T * q.topk;
     if (cudaMemcpyAsync(y_host, at<void>(workspace, q.o_y), T * q.d * 4, cudaMemcpyDeviceToHost,
                         s) != cudaSuccess ||
-        cudaMemcpyAsync(expert_id_host, at<void>(workspace, q.o_eid), T * 4,
+        cudaMemcpyAsync(expert_id_host, at<void>(workspace, q.o_eid), Tk * 4,
                         cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaMemcpyAsync(gate_host, at<void>(workspace, q.o_gate), T * 4, cudaMemcpyDeviceToHost,
+        cudaMemcpyAsync(gate_host, at<void>(workspace, q.o_gate), Tk * 4, cudaMemcpyDeviceToHost,
                         s) != cudaSuccess ||
-        cudaMemcpyAsync(slot_host, at<void>(workspace, q.o_slot), T * 4, cudaMemcpyDeviceToHost,
+        cudaMemcpyAsync(slot_host, at<void>(workspace, q.o_slot), Tk * 4, cudaMemcpyDeviceToHost,
                         s) != cudaSuccess ||
-        cudaMemcpyAsync(drop_mask_host, at<void>(workspace, q.o_drop), T, cudaMemcpyDeviceToHost,
+        cudaMemcpyAsync(drop_mask_host, at<void>(workspace, q.o_drop), Tk, cudaMemcpyDeviceToHost,
                         s) != cudaSuccess)
       return SWITCH_MOE_ERR_CUDA;
   }

@@ -96,7 +96,11 @@ __device__ void finish_experts(const ScanArgs& a, int* sh_i, double* sh_d) {
     if (i < e1) {
       const int c = __ldcg(a.counts + i);
       const float p = __ldcg(a.P_sum + i);
-      const int kept = a.kept ? __ldcg(a.kept + i) : min(c, a.C);
+      int kept = a.kept ? __ldcg(a.kept + i) : min(c, a.C);
+      if (a.counts2) {   // top-2: first choices, then second choices up to C
+        kept = min(a.C, kept + __ldcg(a.counts2 + i));
+        a.kept_out[i] = kept;
+      }
       cv[j] = c;
       nv[j] = (kept + a.BN - 1) / a.BN;
       c_loc += c;
@@ -136,32 +140,39 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __shared__ int is_last;
   grid_dep_wait();
   grid_dep_launch();
-  const int e = blockIdx.x, tid = threadIdx.x;
+  // CTAs N .. 2N-1 (top-2): the second choices' histograms, no probabilities
+  const bool second = blockIdx.x >= a.N;
+  const int e = second ? blockIdx.x - a.N : blockIdx.x, tid = threadIdx.x;
+  int32_t* hist = second ? a.hist2 : a.hist;
   const int per = (a.R + kScanThreads - 1) / kScanThreads;
   const int r0 = min(a.R, tid * per), r1 = min(a.R, r0 + per);
   int cnt = 0;
   float ps = 0.f;
   for (int r = r0; r < r1; ++r) {
-    cnt += a.hist[(size_t)r * a.N + e];
-    ps += a.P_part[(size_t)r * a.N + e];
+    cnt += hist[(size_t)r * a.N + e];
+    if (!second) ps += a.P_part[(size_t)r * a.N + e];
   }
   int total;
   int run = block_exclusive_scan(cnt, &total, sh_i);
   for (int r = r0; r < r1; ++r) {
     const size_t i = (size_t)r * a.N + e;
-    const int v = a.hist[i];
-    a.hist[i] = run;
+    const int v = hist[i];
+    hist[i] = run;
     run += v;
   }
   const float psum = block_sum<float>(ps, sh_f);
   if (tid == 0) {
-    a.counts[e] = total;
-    a.P_sum[e] = psum;
+    if (second) {
+      a.counts2[e] = total;
+    } else {
+      a.counts[e] = total;
+      a.P_sum[e] = psum;
+    }
   }
   if (a.defer_finish) return;   // the slot-assignment kernel runs finish_experts
   if (tid == 0) {
     __threadfence();
-    is_last = (atomicAdd(&a.ctrl[0], 1) == a.N - 1);
+    is_last = (atomicAdd(&a.ctrl[0], 1) == (int)gridDim.x - 1);
   }
   __syncthreads();
   if (!is_last) return;
@@ -221,17 +232,65 @@ __device__ __forceinline__ void stage_row_begin(const AssignArgs& a, uint8_t* bu
     bulk_load(buf, static_cast<const char*>(a.x) + (size_t)t * rb, rb, bar);
   }
 }
+// A second destination (e2, dst_row2 >= 0) takes the same row: top-2.
 __device__ __forceinline__ void stage_row_end(const AssignArgs& a, uint8_t* buf, uint64_t* bar,
-                                              int e, int dst_row, uint32_t rb, int lane) {
+                                              int e, int dst_row, uint32_t rb, int lane,
+                                              int e2 = 0, int dst_row2 = -1) {
   if (lane == 0) {
     // the load must land before the CTA may exit, copied or not
-    if (row_wait(bar, a.status) && dst_row >= 0) {
+    if (row_wait(bar, a.status) && (dst_row >= 0 || dst_row2 >= 0)) {
       fence_proxy_async_smem();
-      bulk_store(static_cast<char*>(a.xbuf) + ((size_t)e * a.C + dst_row) * rb, buf, rb);
+      char* xb = static_cast<char*>(a.xbuf);
+      if (dst_row >= 0) bulk_store(xb + ((size_t)e * a.C + dst_row) * rb, buf, rb);
+      if (dst_row2 >= 0) bulk_store(xb + ((size_t)e2 * a.C + dst_row2) * rb, buf, rb);
       bulk_commit();
       bulk_wait_read();
     }
   }
+}
+
+// Top-2, token order: choice 0 takes slot bases[g][e0] + rank, as in top-1;
+// choice 1 queues behind every first choice its expert kept:
+// slot min(counts[e1], C) + bases2[g][e1] + rank2.  Each is kept iff its
+// slot < C.  The gates are the two probabilities, or renormalised over the
+// pair.  The x row goes to both kept slots; y is zeroed for the atomic
+// accumulation of the two outputs.
+__device__ __forceinline__ void assign_top2(const AssignArgs& a, int t, uint8_t* buf,
+                                            uint64_t* bar, uint32_t rb, bool staged, int lane) {
+  const size_t g = (size_t)(t / kRouterTM) * a.N;
+  const int e0 = a.cand[(size_t)t * kMaxCand], e1 = a.cand[(size_t)t * kMaxCand + 1];
+  const int s0 = a.bases[g + e0] + a.local_rank[t];
+  const int s1 = min(a.counts[e1], a.C) + a.bases2[g + e1] + a.local_rank2[t];
+  const bool k0 = s0 < a.C, k1 = s1 < a.C;
+  if (lane == 0) {
+    float g0 = a.cand_p[(size_t)t * kMaxCand], g1 = a.cand_p[(size_t)t * kMaxCand + 1];
+    if (a.renorm) {
+      const float z = g0 + g1;
+      g0 = g0 / z;
+      g1 = g1 / z;
+    }
+    a.eid_out[2 * (size_t)t] = e0;
+    a.eid_out[2 * (size_t)t + 1] = e1;
+    a.gate_out[2 * (size_t)t] = g0;
+    a.gate_out[2 * (size_t)t + 1] = g1;
+    a.slot[2 * (size_t)t] = k0 ? s0 : -1;
+    a.slot[2 * (size_t)t + 1] = k1 ? s1 : -1;
+    a.drop[2 * (size_t)t] = k0 ? 0 : 1;
+    a.drop[2 * (size_t)t + 1] = k1 ? 0 : 1;
+    if (a.xbuf && a.tok_of_slot) {
+      if (k0) a.tok_of_slot[(size_t)e0 * a.C + s0] = 2 * t;
+      if (k1) a.tok_of_slot[(size_t)e1 * a.C + s1] = 2 * t + 1;
+    }
+  }
+  if (staged) {
+    stage_row_end(a, buf, bar, e0, k0 ? s0 : -1, rb, lane, e1, k1 ? s1 : -1);
+  } else if (a.xbuf) {
+    const char* src = static_cast<const char*>(a.x) + (size_t)t * rb;
+    char* xb = static_cast<char*>(a.xbuf);
+    if (k0) copy_row(src, xb + ((size_t)e0 * a.C + s0) * rb, (int)rb, lane);
+    if (k1) copy_row(src, xb + ((size_t)e1 * a.C + s1) * rb, (int)rb, lane);
+  }
+  if (a.y) zero_row(a.y + (size_t)t * a.d, a.d, lane);
 }
 
 __global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a, ScanArgs sa) {
@@ -252,6 +311,10 @@ __global__ void __launch_bounds__(kRowWarps * 32) assign_kernel(AssignArgs a, Sc
   const bool staged = a.mode == SWITCH_MOE_TOKEN_ORDER && a.xbuf && rb <= kStageRowMax;
   uint8_t* buf = rowbuf + (size_t)warp * rb;
   if (staged) stage_row_begin(a, buf, &rowbar[warp], t, rb, lane);   // x row is known already
+  if (a.topk == 2) {
+    assign_top2(a, t, buf, &rowbar[warp], rb, staged, lane);
+    return;
+  }
   const int e = a.expert_id[t];
   const int s = a.bases[(size_t)(t / kRouterTM) * a.N + e] + a.local_rank[t];
   if (a.mode == SWITCH_MOE_TOKEN_ORDER) {
@@ -541,7 +604,7 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(AssignArgs a) 
 }  // namespace
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl) {
-  return launch_k(scan_kernel, dim3(a.N), dim3(kScanThreads), 0, s, pdl, a);
+  return launch_k(scan_kernel, dim3(a.hist2 ? 2 * a.N : a.N), dim3(kScanThreads), 0, s, pdl, a);
 }
 
 // Dynamic shared memory of the row-staging kernels: one row per warp when

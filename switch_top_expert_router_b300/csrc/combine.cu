@@ -1,8 +1,10 @@
 // Combine: back to token order, gate scale, zero fill for dropped tokens,
 // shared-expert add.
 //
-//   y[t] = (dropped ? 0 : g_t * sum_s O_s[e_t * C + slot_t]) + S[t]
-//   g_t  = gate_t when gate_multiply, else 1
+//   y[t] = sum over the token's kept choices r of g_tr * sum_s O_s[e_tr * C + slot_tr]
+//          (+ S[t]); 0 when every choice was dropped
+//   g_tr = gate_tr when gate_multiply, else 1; one choice for top-1, two for top-2
+//   (the weighted merge of "Top-1 路由 (Top-1 Routing)", comparison section)
 //
 // Sources: "Top-1 路由 (Top-1 Routing)" (compassingai.com), core mechanism
 // step 3 (Switch returns the chosen expert's output unscaled) against the
@@ -29,30 +31,50 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(CombineArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarps + warp;
   if (t >= a.T) return;
-  const int s = a.slot[t];
   const int nv = a.d >> 2;
   float4* y = reinterpret_cast<float4*>(a.y + (size_t)t * a.d);
   const float4* S = a.S ? reinterpret_cast<const float4*>(a.S + (size_t)t * a.d) : nullptr;
-  if (s < 0) {
-    for (int v = lane; v < nv; v += 32) y[v] = S ? __ldg(S + v) : make_float4(0.f, 0.f, 0.f, 0.f);
-    return;
+  const float4* O0 = nullptr;   // the kept choices' expert outputs, in choice order
+  const float4* O1 = nullptr;
+  float g0 = 0.f, g1 = 0.f;
+  for (int r = 0; r < a.topk; ++r) {
+    const size_t i = (size_t)t * a.topk + r;
+    const int s = a.slot[i];
+    if (s < 0) continue;
+    const float4* o = reinterpret_cast<const float4*>(a.O + ((size_t)a.expert_id[i] * a.C + s) * a.d);
+    const float g = a.gate_multiply ? a.gate[i] : 1.0f;
+    if (!O0) {
+      O0 = o;
+      g0 = g;
+    } else {
+      O1 = o;
+      g1 = g;
+    }
   }
-  const int e = a.expert_id[t];
-  const float g = a.gate_multiply ? a.gate[t] : 1.0f;
-  const float4* O = reinterpret_cast<const float4*>(a.O + ((size_t)e * a.C + s) * a.d);
   const size_t ss = a.split_stride >> 2;
-  for (int v = lane; v < nv; v += 32) {
+  auto expert_out = [&](const float4* O, int v) {   // sum of the K-split partials
     float4 acc = __ldg(O + v);
     for (int k = 1; k < a.ksplit; ++k) {
       const float4 o = __ldg(O + k * ss + v);
       acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
     }
-    acc.x *= g; acc.y *= g; acc.z *= g; acc.w *= g;
+    return acc;
+  };
+  for (int v = lane; v < nv; v += 32) {
+    float4 res = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (O0) {
+      const float4 acc = expert_out(O0, v);
+      res = make_float4(g0 * acc.x, g0 * acc.y, g0 * acc.z, g0 * acc.w);
+    }
+    if (O1) {
+      const float4 acc = expert_out(O1, v);
+      res.x += g1 * acc.x; res.y += g1 * acc.y; res.z += g1 * acc.z; res.w += g1 * acc.w;
+    }
     if (S) {
       const float4 sv = __ldg(S + v);
-      acc.x += sv.x; acc.y += sv.y; acc.z += sv.z; acc.w += sv.w;
+      res.x += sv.x; res.y += sv.y; res.z += sv.z; res.w += sv.w;
     }
-    y[v] = acc;
+    y[v] = res;
   }
 }
 

@@ -37,7 +37,7 @@ constexpr int kTileM = 128;          // weight rows per tensor-core tile (MMA M)
 constexpr int kTileK = 64;           // bf16 elements per 128-byte K block
 constexpr int kSimtTileN = 32;       // tokens per fp32 SIMT tile
 constexpr int kMaxExpertsTc = 256;   // experts the tensor-core router takes (one MMA N)
-constexpr int kMaxCand = 4;          // Expanded Drop: candidates per token
+constexpr int kMaxCand = 4;          // Expanded Drop / top-2: candidates per token
 
 // ------------------------------------------------------------------ router
 struct RouterArgs {
@@ -60,6 +60,10 @@ struct RouterArgs {
   int n_cand;
   int32_t* cand;          // [T][kMaxCand]
   float* cand_p;          // [T][kMaxCand]
+  // top-2 (n_cand == 2): histogram and in-group ranks of every token's
+  // second choice cand[1], like hist / local_rank for the first; or null
+  int32_t* hist2;         // [R, N]
+  int32_t* local_rank2;   // [T]
 };
 
 // A token's first kMaxCand experts by logit, descending, lowest index first
@@ -123,6 +127,12 @@ struct ScanArgs {
   // filled slots per expert for the work list (Expanded Drop), or null:
   // min(counts, C)
   const int32_t* kept;
+  // top-2: the second choices' histograms; CTAs N .. 2N-1 scan them into
+  // per-expert bases after the first choices and their totals into counts2;
+  // finish_experts then fills kept_out = min(C, min(counts, C) + counts2)
+  int32_t* hist2;
+  int32_t* counts2;
+  int32_t* kept_out;
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl = false);
 
@@ -145,6 +155,18 @@ struct AssignArgs {
   int32_t* tok_of_slot;        // [N * C] token of each filled slot, or null
   float* y;                    // [T, d] fp32: rows of dropped tokens zeroed, or null
   int* status;
+  // top-2 (topk == 2, token order): each token's two choices come from
+  // cand / cand_p (choice 0 = top-1); expert_id and gate above are unused;
+  // outputs [T, 2] go to eid_out / gate_out and slot / drop; tok_of_slot
+  // holds 2 t + choice; y rows are all zeroed (both choices add into y)
+  int topk;
+  int renorm;                  // gates renormalised over the two choices
+  const int32_t* cand;         // [T][kMaxCand]
+  const float* cand_p;         // [T][kMaxCand]
+  const int32_t* bases2;       // [R, N] scanned second-choice histograms
+  const int32_t* local_rank2;  // [T]
+  int32_t* eid_out;            // [T, 2]
+  float* gate_out;             // [T, 2]
 };
 // Token order: slot, drop and the dispatch copy in one pass.
 // Gate priority: only the per-expert token lists.
@@ -200,6 +222,7 @@ struct GemmArgs {
   int cap;
   int epi;                  // 0: relu -> (bf16 hi, bf16 lo) or fp32; 1: fp32 store;
                             // 2: combine (tensor path): y[tok] = g_tok * D (+ y[tok])
+  int tok_shift;            // epi 2: tok_of_slot holds (token << tok_shift) | choice
   void* out0;               // epi 2: y [T, M] fp32
   void* out1;
   int ldo;                  // output row stride (elements)
@@ -208,7 +231,7 @@ struct GemmArgs {
   const int32_t* tok_of_slot;   // [N * C]
   const float* gate;            // [T]
   int gate_multiply;
-  int y_acc;
+  int y_acc;                // 0: store; 1: add to y (one writer per row); 2: atomic add
   // Tensor path, ksplit == 1: when the last wave of tiles is less than half
   // full, its tiles are cut along K into pieces that run on the idle CTAs;
   // the pieces leave fp32 partials and the last piece of each 32-row slice
@@ -250,9 +273,11 @@ struct FfnArgs {
   __nv_bfloat16* H0;          // [N * C, F] hi
   __nv_bfloat16* H1;          // [N * C, F] lo
   float* y;                   // [T, d]
-  const int32_t* tok_of_slot; // [N * C]
-  const float* gate;          // [T]
-  int gate_multiply, y_acc;
+  const int32_t* tok_of_slot; // [N * C] (token << tok_shift) | choice; gate index
+  const float* gate;          // [T << tok_shift]
+  int tok_shift;
+  int gate_multiply;
+  int y_acc;                  // 0: store; 1: add to y (one writer per row); 2: atomic add
   float* part;                // tail split partials [part_units][128 * BN], or null
   int part_units;
   int32_t* split_cnt;         // [4 * part_units]
@@ -271,6 +296,7 @@ cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap& tmW1, const CUten
 struct CombineArgs {
   int T, d, C, ksplit;
   int gate_multiply;
+  int topk;                 // choices per token (expert_id, gate, slot are [T, topk])
   const int32_t* expert_id;
   const float* gate;
   const int32_t* slot;

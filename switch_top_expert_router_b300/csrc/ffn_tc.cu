@@ -10,7 +10,9 @@
 // where capacity comes from); GEMM 2's epilogue is the combine step (the
 // gate scales the expert output when gate_multiply is set: the Switch
 // Transformer walk-through's Switch layer, Eq. 2, against Top-1 Routing's
-// step 3).  Tile shapes, operand layouts, the hi + lo split of H and the
+// step 3).  With top-2 routing a token's two choices add into its y row
+// with atomic adds (the row starts at zero or at the shared expert's
+// output).  Tile shapes, operand layouts, the hi + lo split of H and the
 // epilogues are those of gemm_tc.cu (swap AB: expert weights are the
 // 128-row MMA M, the expert's tokens the MMA N).
 //
@@ -407,8 +409,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tk = 0;
         gv = 1.f;
         if (c + lane < u.nv) {
-          tk = a.tok_of_slot[out_row0 + (size_t)(c + lane)];
-          if (a.gate_multiply) gv = a.gate[tk];
+          const int code = a.tok_of_slot[out_row0 + (size_t)(c + lane)];
+          tk = code >> a.tok_shift;   // token row; code indexes the gate of this choice
+          if (a.gate_multiply) gv = a.gate[code];
         }
       };
       int tk32 = 0;
@@ -510,7 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_ok && c0 + jj < u.nv) {
               float* dst = a.y + (size_t)tj * (size_t)a.d + row;
               const float val = gj * v[jj >> 4][jj & 15];
-              *dst = a.y_acc ? *dst + val : val;
+              if (a.y_acc == 2) {
+                atomicAdd(dst, val);   // top-2: two choices add into one row
+              } else {
+                *dst = a.y_acc ? *dst + val : val;
+              }
             }
           }
         }

@@ -301,8 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tk = 0;
         gv = 1.f;
         if (c + lane < w.nv) {
-          tk = g.tok_of_slot[out_row0 + (size_t)(c + lane)];
-          if (g.gate_multiply) gv = g.gate[tk];
+          const int code = g.tok_of_slot[out_row0 + (size_t)(c + lane)];
+          tk = code >> g.tok_shift;   // token row; code indexes the gate of this choice
+          if (g.gate_multiply) gv = g.gate[code];
         }
       };
       int tk32 = 0;
@@ -386,7 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_ok && c0 + j < w.nv) {
               float* dst = y + (size_t)tj * (size_t)g.ldo + row;
               const float val = gj * v[j >> 4][j & 15];
-              *dst = g.y_acc ? *dst + val : val;
+              if (g.y_acc == 2) {
+                atomicAdd(dst, val);   // top-2: two choices add into one row
+              } else {
+                *dst = g.y_acc ? *dst + val : val;
+              }
             }
           }
         }

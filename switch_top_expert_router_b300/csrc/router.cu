@@ -100,14 +100,15 @@ __device__ void logits_tile(const XT* __restrict__ x, const float* __restrict__ 
   __syncthreads();
 }
 
-// Softmax / argmax / gate / P partials / histogram / in-CTA rank on lg.
+// Softmax / argmax / gate / P partials / histogram / in-CTA rank on lg (and
+// with top-2 the same histogram and ranks of the second choices).
 // One thread per token runs the row in increasing expert order (the same
 // operation sequence as the tensor-core router's epilogue, so both give
 // bit-identical results on identical logits):
 //   m = max_i l_i, e = first i with l_i == m (lowest index wins ties),
 //   s = sum_i exp(l_i - m) (sequential), gate = 1 / s, p_i = exp(l_i - m) / s.
 __device__ void route_tile(float* lg, int ldl, int T, int N, int t0, int cta,
-                           const RouterArgs& a, int* es, int* hs) {
+                           const RouterArgs& a, int* es, int* es2, int* hs) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid < TM && t0 + tid < T) {
     const int t = t0 + tid;
@@ -128,6 +129,7 @@ __device__ void route_tile(float* lg, int ldl, int T, int N, int t0, int cta,
     a.expert_id[t] = mi;
     a.gate[t] = inv;    // score of the argmax: exp(0) / s
     es[tid] = mi;
+    if (a.hist2) es2[tid] = cand[1];
     for (int r = 0; r < a.n_cand && a.n_cand > 1; ++r) {
       a.cand[(size_t)t * kMaxCand + r] = cand[r];
       a.cand_p[(size_t)t * kMaxCand + r] = row[cand[r]];
@@ -155,6 +157,23 @@ __device__ void route_tile(float* lg, int ldl, int T, int N, int t0, int cta,
   }
   __syncthreads();
   for (int i = tid; i < N; i += NTHREADS) a.hist[(size_t)cta * N + i] = hs[i];
+  if (!a.hist2) return;
+  // top-2: the same for every token's second choice
+  __syncthreads();
+  for (int i = tid; i < N; i += NTHREADS) hs[i] = 0;
+  __syncthreads();
+  if (warp == 0) {
+    const bool valid = lane < nt;
+    const int e = valid ? es2[lane] : -1 - lane;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (valid) {
+      const unsigned lt = (1u << lane) - 1u;
+      a.local_rank2[t0 + lane] = __popc(peers & lt);
+      if ((peers & lt) == 0) hs[e] = __popc(peers);
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < N; i += NTHREADS) a.hist2[(size_t)cta * N + i] = hs[i];
 }
 
 template <typename XT>
@@ -168,7 +187,8 @@ __global__ void __launch_bounds__(NTHREADS) router_kernel(RouterArgs a) {
   float* xs = lg + ((TM * ldl + 3) & ~3);            // [KT][TM + 4]
   float* ws = xs + KT * (TM + 4);                    // [KT][EC + 4]
   int* es = reinterpret_cast<int*>(ws + KT * (EC + 4));  // [TM]
-  int* hs = es + TM;                                 // [N]
+  int* es2 = es + TM;                                // [TM] second choices (top-2)
+  int* hs = es2 + TM;                                // [N]
   const int t0 = blockIdx.x * TM;
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.ctrl) {
     a.ctrl[0] = 0;   // done counter of the scan kernel that follows
@@ -190,13 +210,13 @@ __global__ void __launch_bounds__(NTHREADS) router_kernel(RouterArgs a) {
     }
     return;
   }
-  route_tile(lg, ldl, a.T, a.N, t0, blockIdx.x, a, es, hs);
+  route_tile(lg, ldl, a.T, a.N, t0, blockIdx.x, a, es, es2, hs);
 }
 
 size_t router_smem_bytes(int N) {
   size_t ldl = (size_t)N + 1;
   size_t f = ((TM * ldl + 3) & ~(size_t)3) + KT * (TM + 4) + KT * (EC + 4);
-  return f * sizeof(float) + (TM + (size_t)N) * sizeof(int);
+  return f * sizeof(float) + (2 * TM + (size_t)N) * sizeof(int);
 }
 
 }  // namespace

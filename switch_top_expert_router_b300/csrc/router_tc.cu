@@ -77,6 +77,25 @@ constexpr int kRegExperts = 128;   // experts whose running sums fit in register
 constexpr int kEpiLd = kRegExperts + 1;
 constexpr size_t kEpiBytes = (size_t)128 * kEpiLd * 4 + 128 * 4;   // logits + 1 / sums
 
+// top-2: histogram and in-group ranks of one 32-token group's second
+// choices e2 (-1 - lane past T), through this warp's histogram hs, which
+// holds the first choices' histogram on entry (already stored).
+__device__ __noinline__ void second_choice_hist(const RouterArgs& a, int* hs, int e2, bool valid,
+                                                int lane, int t, int g) {
+  const int N = a.N;
+  __syncwarp();
+  for (int i = lane; i < N; i += 32) hs[i] = 0;
+  __syncwarp();
+  const unsigned peers = __match_any_sync(0xffffffffu, e2);
+  if (valid) {
+    const unsigned lt = (1u << lane) - 1u;
+    a.local_rank2[t] = __popc(peers & lt);
+    if ((peers & lt) == 0) hs[e2] = __popc(peers);
+  }
+  __syncwarp();
+  for (int i = lane; i < N; i += 32) a.hist2[(size_t)g * N + i] = hs[i];
+}
+
 // Routing of one epilogue warp's 32 tokens from their logits, staged in
 // shared memory (row r = token t0 + r): expert id, gate, the group's
 // per-expert probability sums and its histogram plus in-group ranks.  Each
@@ -146,6 +165,7 @@ __device__ __noinline__ void route_group_smem(const RouterArgs& a, float* lg, fl
   }
   __syncwarp();
   for (int i = lane; i < N; i += 32) a.hist[(size_t)g * N + i] = hs[i];
+  if (a.hist2) second_choice_hist(a, hs, valid ? cand[1] : -1 - lane, valid, lane, t, g);
 }
 
 // Epilogue warps for N <= kRegExperts: promote every K block's TMEM sum
@@ -421,9 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.expert_id[t] = mi;
         a.gate[t] = inv;
       }
+      int c2 = -1;   // second choice (top-2)
       if (!a.logits_out && a.n_cand > 1) {
-        // Expanded Drop candidates: one more pass over the TMEM row with the
-        // insertion of topk_candidates
+        // Expanded Drop / top-2 candidates: one more pass over the TMEM row
+        // with the insertion of topk_candidates
         int cand[kMaxCand];
         float cl[kMaxCand];
 #pragma unroll
@@ -460,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             a.cand_p[(size_t)t * kMaxCand + r] = expf(cl[r] - m) * inv;
           }
         }
+        c2 = cand[1];
       }
       // pass 3, 32 experts at a time: probabilities through this warp's
       // [32][33] slice of the (now idle) pipeline buffers, then the group's
@@ -503,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         for (int i = lane; i < N; i += 32) a.hist[(size_t)g * N + i] = hs[i];
+        if (a.hist2) second_choice_hist(a, hs, valid ? c2 : -1 - lane, valid, lane, t, g);
       }
     }
     }   // !kRegs

@@ -660,3 +660,20 @@ def test_forward_top2_zero_second_expert_is_top1():
         np.testing.assert_allclose(a["y"], b["y"], rtol=1e-13, atol=1e-13)
         assert np.array_equal(a["slot"][:, 0], b["slot"])
         assert a["aux_loss"] == b["aux_loss"]
+
+
+def test_forward_rows_top2_matches_forward_top2():
+    rng = np.random.default_rng(16)
+    T, d, F, N = 80, 8, 12, 6
+    x = torch.tensor(rng.normal(size=(T, d)))
+    W_g = torch.tensor(rng.normal(size=(N, d)))
+    W1 = torch.tensor(rng.normal(size=(N, F, d)))
+    W2 = torch.tensor(rng.normal(size=(N, d, F)))
+    W1s = torch.tensor(rng.normal(size=(F, d)))
+    W2s = torch.tensor(rng.normal(size=(d, F)))
+    full = O.forward_top2(x, W_g, W1, W2, 0.7, gate_multiply=1, renormalize=1, W1s=W1s, W2s=W2s)
+    assert 0 < full["drop"].sum() < 2 * T
+    rows = rng.choice(T, 30, replace=False)
+    part = O.forward_rows_top2(rows, x, full["expert_id"], full["gate"], full["slot"], 1,
+                               lambda e: (W1[e], W2[e]), W1s, W2s)
+    np.testing.assert_allclose(part, full["y"][rows], rtol=1e-12, atol=1e-12)
