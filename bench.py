@@ -165,17 +165,30 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle sample
-def oracle_sample_step(w, seed=0, expand=1):
+def oracle_sample_step(w, seed=0, expand=1, top_k=1, renormalize=0):
     """One bounded CPU-oracle step on the workload: route the whole batch
-    (with Expanded Drop over `expand` candidates when > 1), then the expert
-    FFN and combine of the tokens processed by the first CPU_SAMPLE_EXPERTS
-    experts.  Returns (tokens processed, seconds)."""
+    (with Expanded Drop over `expand` candidates when > 1, or top-2), then the
+    expert FFN and combine of the tokens processed by the first
+    CPU_SAMPLE_EXPERTS experts (top-2: of the token-choice pairs, counted as
+    half a token each).  Returns (tokens processed, seconds)."""
     import oracle
     inp = make_inputs(w, seed, device="cpu", with_experts=False)
     experts = {e: expert_weights(w, e, seed, "cpu") for e in range(min(CPU_SAMPLE_EXPERTS, w.N))}
     t0 = time.perf_counter()
     r = oracle.route(inp.x, inp.W_g, zipf_bias(w))
     C = oracle.capacity(w.T, w.N, w.capacity_factor)
+    if top_k == 2:
+        c = oracle.candidates(r["logits"], 2)
+        g2 = oracle.top2_gates(r["probs"], c, renormalize)
+        s2, _, _ = oracle.assign_slots_top2(c, w.N, C)
+        pairs = 0
+        for k in range(2):
+            rows = np.nonzero(c[:, k] < len(experts))[0]
+            oracle.forward_rows(rows, inp.x, c[:, k], g2[:, k], s2[:, k], w.gate_multiply,
+                                lambda i: experts[i])
+            pairs += int(rows.size)
+        oracle.aux_loss(r["probs"], np.bincount(c[:, 0], minlength=w.N))
+        return pairs / 2, time.perf_counter() - t0
     slot, drop, counts = oracle.assign_slots(r["expert_id"], r["gate"], w.N, C, w.priority_mode)
     e, g = r["expert_id"], r["gate"]
     if expand > 1:
@@ -213,10 +226,11 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     for _ in range(args.warmup):
-        oracle_sample_step(w, expand=args.expand)
+        oracle_sample_step(w, expand=args.expand, top_k=args.top_k, renormalize=args.renormalize)
     tok, sec = 0, 0.0
     for _ in range(args.steps):
-        n, s = oracle_sample_step(w, expand=args.expand)
+        n, s = oracle_sample_step(w, expand=args.expand, top_k=args.top_k,
+                                  renormalize=args.renormalize)
         tok += n
         sec += s
     value = tok / sec
@@ -226,7 +240,7 @@ def run_reference(args, rank, world):
         "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, args.expand),
+        "config": workload_config(w, args.expand, args.top_k, args.renormalize),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": cpu_sample_desc(w)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -235,12 +249,14 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w, expand=1):
-    return {"workload": f"{w.name}: Switch top-1 MoE layer T={w.T} d_model={w.d_model} "
+def workload_config(w, expand=1, top_k=1, renormalize=0):
+    route = ("top-2" + (" (gates renormalised over the pair)" if renormalize else "")
+             if top_k == 2 else "Switch top-1")
+    return {"workload": f"{w.name}: {route} MoE layer T={w.T} d_model={w.d_model} "
                         f"d_ff={w.d_ff} N={w.N} cf={w.capacity_factor} {w.dtype}"
                         f"{' +shared expert' if w.has_shared else ''}"
                         f"{f' +Expanded Drop over {expand} candidates' if expand > 1 else ''}",
-            "expanded_drop_candidates": expand,
+            "expanded_drop_candidates": expand, "top_k": top_k,
             "T": w.T, "d_model": w.d_model, "d_ff": w.d_ff, "N": w.N,
             "capacity_factor": w.capacity_factor,
             "priority": "gate" if w.priority_mode else "token-order",
@@ -261,6 +277,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--expand", type=int, default=1,
                     help="Expanded Drop: candidates per token (1 = plain top-1)")
+    ap.add_argument("--top-k", type=int, default=1, choices=[1, 2],
+                    help="experts per token (2: top-2 token choice)")
+    ap.add_argument("--renormalize", type=int, default=0, choices=[0, 1],
+                    help="top-2 gates renormalised over the chosen pair")
     ap.add_argument("--token-order", action="store_true",
                     help="token-order priority whatever the workload's (Expanded Drop "
                          "on the skewed shape)")
@@ -289,7 +309,7 @@ def main():
     inp = make_inputs(w, seed=0, device=dev)
     p = sm.make_params(w.T, w.d_model, w.d_ff, w.N, w.capacity_factor, w.priority_mode,
                        w.gate_multiply, sm.BF16 if w.dtype == "bf16" else sm.F32, w.has_shared,
-                       args.expand)
+                       args.expand, args.top_k, args.renormalize)
     ws = sm.workspace(sm.switch_moe_workspace_bytes(p), dev)
     out = None
     stream = torch.cuda.current_stream(dev)
@@ -299,7 +319,8 @@ def main():
         out = sm.switch_moe_forward(inp.x, inp.W_g, inp.W1, inp.W2, w.capacity_factor,
                                     w.priority_mode, w.gate_multiply, b_g=inp.b_g,
                                     W1s=inp.W1s, W2s=inp.W2s, ws=ws, out=out,
-                                    expand=args.expand)
+                                    expand=args.expand, top_k=args.top_k,
+                                    renormalize=args.renormalize)
 
     for _ in range(args.warmup):
         step()
@@ -353,7 +374,8 @@ def main():
     eid, slt = out.expert_id.cpu().numpy(), out.slot.cpu().numpy()
     kept = np.bincount(eid[slt >= 0], minlength=w.N).astype(np.int64)
     active = int((kept > 0).sum())
-    T_kept = int(kept.sum())
+    T_kept = int(kept.sum())   # filled slots (top-2: token-choice pairs)
+    out_rows = int((slt.reshape(w.T, -1) >= 0).any(axis=1).sum())   # y rows written
     eb = 2 if w.dtype == "bf16" else 4
     d, F = w.d_model, w.d_ff
     wbytes_expert = d * F * eb
@@ -367,11 +389,11 @@ def main():
     # weights, the dispatched tokens in and the expert outputs out -- and,
     # when GEMM 1 and GEMM 2 are separate launches, H out of one and into the
     # other (the mean of the two launches)
-    ffn_bytes = (2 * active * wbytes_expert + T_kept * d * eb + T_kept * d * 4 if ffn_one
+    ffn_bytes = (2 * active * wbytes_expert + T_kept * d * eb + out_rows * d * 4 if ffn_one
                  else (g1_bytes + g2_bytes) / 2)
     hbm, bf16_peak, peak_kind = peaks()
     achieved = ffn_bytes * (1 if ffn_one else 2) / (gemm_ms / 1e3) / 1e9
-    layer_bytes = (w.T * d * eb + w.T * d * 4 + w.N * d * 4 + w.T * 13 + w.N * 4
+    layer_bytes = (w.T * d * eb + w.T * d * 4 + w.N * d * 4 + w.T * 13 * args.top_k + w.N * 4
                    + 2 * active * wbytes_expert + (2 * wbytes_expert if w.has_shared else 0))
     layer_flops = 4.0 * T_kept * d * F + (4.0 * w.T * d * F if w.has_shared else 0.0)
     t_roof = max(layer_flops / (bf16_peak * 1e12), layer_bytes / (hbm * 1e9))
@@ -396,7 +418,8 @@ def main():
                                                 w.capacity_factor, w.priority_mode,
                                                 w.gate_multiply, b_g=inp.b_g, W1s=inp.W1s,
                                                 W2s=inp.W2s, ws=hws, out=hout,
-                                                expand=args.expand)
+                                                expand=args.expand, top_k=args.top_k,
+                                                renormalize=args.renormalize)
         for _ in range(args.warmup):
             hstep()
         torch.cuda.synchronize()
@@ -412,7 +435,7 @@ def main():
         hms = max_over_ranks(h0.elapsed_time(h1), pg, dev)
         e2e = {"value": job_tokens_per_s(w.T, args.steps, world, hms), "unit": "tokens/s",
                "h2d_bytes_per_step": w.T * d * eb,
-               "d2h_bytes_per_step": w.T * d * 4 + w.T * 13 + w.N * 4 + 4,
+               "d2h_bytes_per_step": w.T * d * 4 + w.T * 13 * args.top_k + w.N * 4 + 4,
                "ms_per_step": hms / args.steps}
         if sm.switch_moe_sync_status() != 0:
             raise RuntimeError("device status after the host-IO run")
@@ -421,7 +444,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tok, sec = 0, 0.0
         while sec < 10.0:
-            n, s = oracle_sample_step(w, expand=args.expand)
+            n, s = oracle_sample_step(w, expand=args.expand, top_k=args.top_k,
+                                      renormalize=args.renormalize)
             tok += n
             sec += s
         cpu = {"value": tok / sec, "unit": "tokens/s", "cores": blas_threads(),
@@ -433,14 +457,17 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": workload_config(w, args.expand),
+            "config": workload_config(w, args.expand, args.top_k, args.renormalize),
             "e2e": e2e,
             "roofline": {"kernel": ("ffn_tc_kernel (expert GEMM 1 + 2, one launch)" if ffn_one
                                     else "gemm_tc_kernel (expert GEMM 1 + 2)"),
                          "bound": "hbm",
                          "achieved": achieved, "peak": hbm, "unit": "GB/s",
                          "frac": achieved / hbm, "peak_kind": peak_kind,
-                         "traffic": kernel_traffic(args.config) if ffn_one else None,
+                         # the ncu figure is for the plain top-1 workload only
+                         "traffic": (kernel_traffic(args.config)
+                                     if ffn_one and args.expand == 1 and args.top_k == 1
+                                     else None),
                          "algorithmic_bytes_per_launch": ffn_bytes},
             "layer_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": 1e3 * ms / args.steps,
                                "frac": t_roof / (ms / args.steps / 1e3),
@@ -448,8 +475,10 @@ def main():
                                "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16_peak,
                                          "kind": peak_kind}},
             "phase_us": {k: 1e3 * v for k, v in phase_ms.items()},
-            "routing": {"active_experts": active, "kept_tokens": T_kept,
-                        "dropped": int(w.T - T_kept), "capacity": C,
+            "routing": {"active_experts": active,
+                        # top-2: token-choice pairs kept and dropped
+                        "kept_tokens": T_kept, "dropped": int(w.T * args.top_k - T_kept),
+                        "capacity": C,
                         "aux_loss": float(out.aux_loss.item())},
             "cpu_baseline": cpu,
             "gpu_launches": launches * args.steps,
