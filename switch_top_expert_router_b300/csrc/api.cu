@@ -407,7 +407,6 @@ int run_gemm(const Plan& q, const DeviceInfo* dev, bool dense, int layer, const 
     g.tok_of_slot = at<int32_t>(ws, q.o_tok);
     g.gate = gate;
     g.gate_multiply = q.gm;
-    g.tok_shift = q.topk - 1;
     // top-2: two choices add into a row (zeroed, or holding the shared
     // expert's output); top-1: the shared expert's output is already in y
     g.y_acc = q.topk == 2 ? 2 : q.shared;
@@ -482,7 +481,7 @@ int run_ffn(const Plan& q, const DeviceInfo* dev, const void* W1, const void* W2
   a.n_experts = (int)q.N;
   a.H0 = at<__nv_bfloat16>(ws, q.o_H0); a.H1 = at<__nv_bfloat16>(ws, q.o_H1);
   a.y = y; a.tok_of_slot = at<int32_t>(ws, q.o_tok); a.gate = gate;
-  a.gate_multiply = q.gm; a.tok_shift = q.topk - 1;
+  a.gate_multiply = q.gm;
   a.y_acc = q.topk == 2 ? 2 : q.shared;
   a.part = at<float>(ws, q.o_part); a.part_units = q.part_units;
   a.split_cnt = at<int32_t>(ws, q.o_splitcnt);

@@ -222,7 +222,6 @@ struct GemmArgs {
   int cap;
   int epi;                  // 0: relu -> (bf16 hi, bf16 lo) or fp32; 1: fp32 store;
                             // 2: combine (tensor path): y[tok] = g_tok * D (+ y[tok])
-  int tok_shift;            // epi 2: tok_of_slot holds (token << tok_shift) | choice
   void* out0;               // epi 2: y [T, M] fp32
   void* out1;
   int ldo;                  // output row stride (elements)
@@ -231,7 +230,9 @@ struct GemmArgs {
   const int32_t* tok_of_slot;   // [N * C]
   const float* gate;            // [T]
   int gate_multiply;
-  int y_acc;                // 0: store; 1: add to y (one writer per row); 2: atomic add
+  // 0: store; 1: add to y (one writer per row); 2: top-2, tok_of_slot holds
+  // 2 token + choice and both choices add into y atomically
+  int y_acc;
   // Tensor path, ksplit == 1: when the last wave of tiles is less than half
   // full, its tiles are cut along K into pieces that run on the idle CTAs;
   // the pieces leave fp32 partials and the last piece of each 32-row slice
@@ -273,11 +274,12 @@ struct FfnArgs {
   __nv_bfloat16* H0;          // [N * C, F] hi
   __nv_bfloat16* H1;          // [N * C, F] lo
   float* y;                   // [T, d]
-  const int32_t* tok_of_slot; // [N * C] (token << tok_shift) | choice; gate index
-  const float* gate;          // [T << tok_shift]
-  int tok_shift;
+  const int32_t* tok_of_slot; // [N * C] token, or 2 token + choice (y_acc 2); gate index
+  const float* gate;          // [T] or [T, 2]
   int gate_multiply;
-  int y_acc;                  // 0: store; 1: add to y (one writer per row); 2: atomic add
+  // 0: store; 1: add to y (one writer per row); 2: top-2, both choices add
+  // into y atomically
+  int y_acc;
   float* part;                // tail split partials [part_units][128 * BN], or null
   int part_units;
   int32_t* split_cnt;         // [4 * part_units]

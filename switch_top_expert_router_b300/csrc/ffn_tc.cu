@@ -134,6 +134,9 @@ __device__ bool wait_count(const int32_t* cnt, int target, volatile int* abort_f
   return false;
 }
 
+// kAtomicY: top-2, each choice adds into its token's y row atomically
+// (a separate instantiation: the combine loop's code size costs time).
+template <bool kAtomicY>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX,
                   const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH0,
@@ -410,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         gv = 1.f;
         if (c + lane < u.nv) {
           const int code = a.tok_of_slot[out_row0 + (size_t)(c + lane)];
-          tk = code >> a.tok_shift;   // token row; code indexes the gate of this choice
+          tk = kAtomicY ? code >> 1 : code;   // token row; code indexes the gate of this choice
           if (a.gate_multiply) gv = a.gate[code];
         }
       };
@@ -513,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_ok && c0 + jj < u.nv) {
               float* dst = a.y + (size_t)tj * (size_t)a.d + row;
               const float val = gj * v[jj >> 4][jj & 15];
-              if (a.y_acc == 2) {
+              if constexpr (kAtomicY) {
                 atomicAdd(dst, val);   // top-2: two choices add into one row
               } else {
                 *dst = a.y_acc ? *dst + val : val;
@@ -554,12 +557,12 @@ size_t ffn_tc_smem_bytes(int BN, int stages) {
 cudaError_t launch_ffn_tc(const FfnArgs& a, const CUtensorMap& tmW1, const CUtensorMap& tmX,
                           const CUtensorMap& tmW2, const CUtensorMap& tmH0,
                           const CUtensorMap& tmH1, cudaStream_t s, bool pdl) {
-  cudaError_t err = cudaFuncSetAttribute(ffn_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = a.y_acc == 2 ? ffn_tc_kernel<true> : ffn_tc_kernel<false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)a.smem_bytes);
   if (err != cudaSuccess) return err;
-  return launch_k(ffn_tc_kernel, dim3(a.grid), dim3(kThreads), a.smem_bytes, s, pdl, tmW1, tmX,
-                  tmW2, tmH0, tmH1, a);
+  return launch_k(kern, dim3(a.grid), dim3(kThreads), a.smem_bytes, s, pdl, tmW1, tmX, tmW2,
+                  tmH0, tmH1, a);
 }
 
 }  // namespace smoe

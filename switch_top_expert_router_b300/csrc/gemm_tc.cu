@@ -134,7 +134,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
 }
 
 // kEpi: the epilogue (GemmArgs::epi), fixed at compile time so each variant
-// carries only its own store path.
+// carries only its own store path; 3 is the combine of top-2 routing (slot
+// codes 2 t + choice, atomic adds into y).
 template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -302,13 +303,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         gv = 1.f;
         if (c + lane < w.nv) {
           const int code = g.tok_of_slot[out_row0 + (size_t)(c + lane)];
-          tk = code >> g.tok_shift;   // token row; code indexes the gate of this choice
+          tk = kEpi == 3 ? code >> 1 : code;   // token row; code indexes the gate of this choice
           if (g.gate_multiply) gv = g.gate[code];
         }
       };
       int tk32 = 0;
       float gv32 = 1.f;
-      if (kEpi == 2 && w.unit < 0) tok_gate(0, tk32, gv32);   // overlaps the wait below
+      if (kEpi >= 2 && w.unit < 0) tok_gate(0, tk32, gv32);   // overlaps the wait below
       // tcgen05.ld below is warp-collective: leave the loop together or not at all
       const bool ready =
           mbar_wait(&tfull[acc], acc_par, abort_flag, status, SWITCH_MOE_ERR_DEVICE_TIMEOUT);
@@ -344,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         from_tmem = false;
         p0 = g.part + (size_t)w.sidx * w.pieces * tile_elems + q * 32 + lane;
-        if (kEpi == 2) tok_gate(0, tk32, gv32);
+        if (kEpi >= 2) tok_gate(0, tk32, gv32);
       }
       // 16 columns c0 .. c0 + 15 of this thread's row into v
       auto fetch16 = [&](int c0, float (&v)[16]) {
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
 
-      if constexpr (kEpi == 2) {
+      if constexpr (kEpi >= 2) {
         // combine: y[token] = g_token * D (+ y[token]), 32 columns per step
         float* y = static_cast<float*>(g.out0);
         for (int c0 = 0; c0 < w.nv; c0 += 32) {
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_ok && c0 + j < w.nv) {
               float* dst = y + (size_t)tj * (size_t)g.ldo + row;
               const float val = gj * v[j >> 4][j & 15];
-              if (g.y_acc == 2) {
+              if constexpr (kEpi == 3) {
                 atomicAdd(dst, val);   // top-2: two choices add into one row
               } else {
                 *dst = g.y_acc ? *dst + val : val;
@@ -453,7 +454,10 @@ size_t gemm_tc_smem_bytes(int BN, int num_b, int stages) {
 
 cudaError_t launch_gemm_tc(const GemmArgs& g, const CUtensorMap& tmA, const CUtensorMap& tmB0,
                            const CUtensorMap& tmB1, cudaStream_t s, bool pdl) {
-  auto kern = g.epi == 0 ? gemm_tc_kernel<0> : g.epi == 1 ? gemm_tc_kernel<1> : gemm_tc_kernel<2>;
+  auto kern = g.epi == 0   ? gemm_tc_kernel<0>
+              : g.epi == 1 ? gemm_tc_kernel<1>
+              : g.y_acc == 2 ? gemm_tc_kernel<3>   // combine with atomic adds (top-2)
+                             : gemm_tc_kernel<2>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_bytes);
   if (err != cudaSuccess) return err;
