@@ -59,7 +59,8 @@ __all__ = [
     "capacity", "router_logits", "softmax", "top1", "route", "route_from_logits",
     "assign_slots", "expert_ffn", "aux_loss", "combine_token", "forward",
     "forward_rows", "candidates", "assign_slots_expanded", "top2_gates",
-    "assign_slots_top2", "forward_top2", "forward_rows_top2",
+    "assign_slots_top2", "forward_top2", "forward_rows_top2", "expert_choice",
+    "forward_expert_choice", "forward_rows_expert_choice",
 ]
 
 TOKEN_ORDER = 0
@@ -287,6 +288,66 @@ def assign_slots_top2(cands, N: int, C: int):
 
 
 # --------------------------------------------------------------------------
+# Expert choice, the paradigm the pages set against token choice:
+#   [TOP1] routing-paradigm table (each expert selects its top-K tokens,
+#   balanced by construction), milestone table (Expert Choice Routing,
+#   Zhou et al. 2022: the choice flips from tokens to experts) and the
+#   comparison table (a token can be taken by several experts, or by none).
+# Readings, none of them printed on the pages:
+#   * the scores are the router of the top-1 layer: s[t, e] = softmax over
+#     the N experts of token t's logits;
+#   * each expert takes k = C = ceil(cf * T / N) tokens (all T when C >= T):
+#     the highest s[:, e], the lower token index first among equal scores;
+#     slot = rank in that order;
+#   * y_t = sum over the experts that took t of s[t, e] * E_e(x_t) (the gate
+#     flag as for top-1); a token no expert took gets 0 (plus the shared
+#     expert);
+#   * expert_counts and L_aux describe the router's top-1 choice, as for the
+#     other variants (expert choice itself needs no balancing loss).
+# --------------------------------------------------------------------------
+def expert_choice(probs, C: int):
+    """Returns (chosen int64 [N, min(C, T)]: each expert's tokens, best
+    first; gates float64 [N, min(C, T)]: their scores)."""
+    p = _f64(probs)
+    T, N = p.shape
+    k = min(C, T)
+    chosen = np.zeros((N, k), dtype=np.int64)
+    gates = np.zeros((N, k), dtype=np.float64)
+    tok = np.arange(T)
+    for e in range(N):
+        order = np.lexsort((tok, -p[:, e]))   # score desc, then token asc
+        chosen[e] = order[:k]
+        gates[e] = p[order[:k], e]
+    return chosen, gates
+
+
+def forward_expert_choice(x, W_g, W1, W2, capacity_factor: float, gate_multiply: int = 1,
+                          b_g=None, W1s=None, W2s=None,
+                          expert_getter: Optional[Callable[[int], tuple]] = None):
+    """The layer with expert-choice routing.  Returns a dict with y (fp64
+    [T, d]), chosen / gates [N, min(C, T)], experts_per_token [T], counts
+    of the router's top-1 choice and aux_loss."""
+    r = route(x, W_g, b_g)
+    T, N = r["probs"].shape
+    C = capacity(T, N, capacity_factor)
+    chosen, gates = expert_choice(r["probs"], C)
+    d = x.shape[1]
+    y = np.zeros((T, d), dtype=np.float64)
+    for e in range(N):
+        W1_e, W2_e = expert_getter(e) if expert_getter else (W1[e], W2[e])
+        o = expert_ffn(_rows(x, chosen[e]), W1_e, W2_e)
+        g = gates[e][:, None] if gate_multiply else 1.0
+        np.add.at(y, chosen[e], g * o)          # one token may be taken by several experts
+    if W1s is not None:
+        y = y + expert_ffn(x, W1s, W2s)
+    per_token = np.bincount(chosen.ravel(), minlength=T).astype(np.int64)
+    counts = np.bincount(r["expert_id"], minlength=N).astype(np.int64)
+    return {"y": y, "chosen": chosen, "gates": gates, "experts_per_token": per_token,
+            "counts": counts, "aux_loss": aux_loss(r["probs"], counts),
+            "logits": r["logits"], "probs": r["probs"], "capacity": C}
+
+
+# --------------------------------------------------------------------------
 # Step a6/a7: the expert, a two-layer bias-free FFN ([TOP1] key-parameter
 # section: about 2 * d_model * d_ff weights per expert).  ReLU between.
 #   W1_e: [d_ff, d_model], W2_e: [d_model, d_ff] (out-features first).
@@ -436,6 +497,33 @@ def forward_rows_top2(rows: Sequence[int], x, expert_id, gate, slot, gate_multip
                          W1s, W2s)
     second = forward_rows(rows, x, e[:, 1], g[:, 1], s[:, 1], gate_multiply, expert_getter)
     return first + second
+
+
+def forward_rows_expert_choice(rows: Sequence[int], x, chosen, gates, gate_multiply: int,
+                               expert_getter: Callable[[int], tuple], W1s=None,
+                               W2s=None) -> np.ndarray:
+    """y for a sample of tokens under given expert-choice decisions
+    (chosen / gates [N, k]): each sampled token's sum over the experts that
+    took it."""
+    rows = np.asarray(rows, dtype=np.int64)
+    chosen = np.asarray(chosen)
+    gates = np.asarray(gates, dtype=np.float64)
+    d = x.shape[1]
+    xr = _rows(x, rows)
+    out = np.zeros((rows.size, d), dtype=np.float64)
+    where = {int(t): k for k, t in enumerate(rows)}
+    for e in range(chosen.shape[0]):
+        hit = [(where[int(t)], g) for t, g in zip(chosen[e], gates[e]) if int(t) in where]
+        if not hit:
+            continue
+        W1_e, W2_e = expert_getter(e)
+        ks = np.array([k for k, _ in hit])
+        o = expert_ffn(xr[ks], W1_e, W2_e)
+        g = np.array([g for _, g in hit])[:, None] if gate_multiply else 1.0
+        np.add.at(out, ks, g * o)
+    if W1s is not None:
+        out = out + expert_ffn(xr, W1s, W2s)
+    return out
 
 
 def _rows(x, rows):

@@ -677,3 +677,103 @@ def test_forward_rows_top2_matches_forward_top2():
     part = O.forward_rows_top2(rows, x, full["expert_id"], full["gate"], full["slot"], 1,
                                lambda e: (W1[e], W2[e]), W1s, W2s)
     np.testing.assert_allclose(part, full["y"][rows], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------ Expert choice
+def _golden_expert_choice():
+    rows, scores = [], None
+    for line in open(os.path.join(GOLDEN, "expert_choice.txt")):
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        if line.startswith("scores"):
+            f = line.split()
+            scores = np.array([[float(v) for v in c.split(",")] for c in f[2:]])
+            continue
+        c, e0, e1, per = (part.split() for part in line.split("|"))
+        rows.append((scores, int(c[0]), [int(v) for v in e0], [int(v) for v in e1],
+                     [int(v) for v in per]))
+    return rows
+
+
+@pytest.mark.parametrize("case", _golden_expert_choice(), ids=lambda c: f"C{c[1]}")
+def test_expert_choice_golden(case):
+    scores, C, want0, want1, want_per = case
+    chosen, gates = O.expert_choice(scores, C)
+    assert chosen[0].tolist() == want0 and chosen[1].tolist() == want1
+    assert np.bincount(chosen.ravel(), minlength=scores.shape[0]).tolist() == want_per
+    for e in range(2):
+        assert np.array_equal(gates[e], scores[chosen[e], e])
+
+
+def test_expert_choice_brute_force_definition():
+    """Token t is in expert e's list iff fewer than C tokens beat it
+    (higher score, or equal score and lower index); its slot is that number."""
+    rng = np.random.default_rng(21)
+    for T, N in [(7, 3), (12, 2), (30, 5)]:
+        s = rng.integers(0, 4, size=(T, N)).astype(np.float64)   # many ties
+        for C in range(1, T + 2):
+            chosen, _ = O.expert_choice(s, C)
+            for e in range(N):
+                for t in range(T):
+                    beat = sum(1 for u in range(T)
+                               if s[u, e] > s[t, e] or (s[u, e] == s[t, e] and u < t))
+                    if beat < C:
+                        assert chosen[e, beat] == t
+                    else:
+                        assert t not in chosen[e].tolist()
+
+
+def test_expert_choice_invariants():
+    rng = np.random.default_rng(22)
+    T, N = 300, 8
+    p = O.softmax(rng.normal(size=(T, N)))
+    for C in (1, 10, 37, 300, 400):
+        chosen, gates = O.expert_choice(p, C)
+        assert chosen.shape == (N, min(C, T))
+        for e in range(N):
+            assert len(set(chosen[e].tolist())) == min(C, T)          # no token twice
+            assert np.all(np.diff(gates[e]) <= 0)                     # best first
+            rest = np.setdiff1d(np.arange(T), chosen[e])
+            if rest.size:
+                assert p[rest, e].max() <= gates[e].min()              # nobody left is better
+        per = np.bincount(chosen.ravel(), minlength=T)
+        assert per.sum() == N * min(C, T) and per.max() <= N
+
+
+def test_forward_expert_choice_closed_forms():
+    """C >= T: every expert takes every token, y = sum_e s[t, e] E_e(x); with
+    identical experts that is E(x) (scores sum to 1) and N E(x) unscaled."""
+    rng = np.random.default_rng(23)
+    T, d, F, N = 24, 10, 16, 4
+    x = torch.tensor(rng.normal(size=(T, d)))
+    W_g = torch.tensor(rng.normal(size=(N, d)))
+    w1 = torch.tensor(rng.normal(size=(F, d)) / np.sqrt(d))
+    w2 = torch.tensor(rng.normal(size=(d, F)) / np.sqrt(F))
+    W1, W2 = w1.expand(N, F, d).clone(), w2.expand(N, d, F).clone()
+    E = torch.nn.functional.linear(torch.relu(torch.nn.functional.linear(x, w1)), w2).numpy()
+    out = O.forward_expert_choice(x, W_g, W1, W2, float(N), gate_multiply=1)
+    assert np.all(out["experts_per_token"] == N)
+    np.testing.assert_allclose(out["y"], E, rtol=1e-12, atol=1e-12)
+    out = O.forward_expert_choice(x, W_g, W1, W2, float(N), gate_multiply=0)
+    np.testing.assert_allclose(out["y"], N * E, rtol=1e-12, atol=1e-12)
+    # cf small: tokens nobody took get exactly zero
+    out = O.forward_expert_choice(x, W_g, W1, W2, 0.25, gate_multiply=1)
+    none = out["experts_per_token"] == 0
+    assert none.any() and np.all(out["y"][none] == 0)
+
+
+def test_forward_rows_expert_choice_matches_forward():
+    rng = np.random.default_rng(24)
+    T, d, F, N = 60, 8, 12, 5
+    x = torch.tensor(rng.normal(size=(T, d)))
+    W_g = torch.tensor(rng.normal(size=(N, d)))
+    W1 = torch.tensor(rng.normal(size=(N, F, d)))
+    W2 = torch.tensor(rng.normal(size=(N, d, F)))
+    W1s = torch.tensor(rng.normal(size=(F, d)))
+    W2s = torch.tensor(rng.normal(size=(d, F)))
+    full = O.forward_expert_choice(x, W_g, W1, W2, 1.3, W1s=W1s, W2s=W2s)
+    rows = rng.choice(T, 25, replace=False)
+    part = O.forward_rows_expert_choice(rows, x, full["chosen"], full["gates"], 1,
+                                        lambda e: (W1[e], W2[e]), W1s, W2s)
+    np.testing.assert_allclose(part, full["y"][rows], rtol=1e-12, atol=1e-12)
