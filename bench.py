@@ -165,7 +165,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ oracle sample
-def oracle_sample_step(w, seed=0, expand=1, top_k=1, renormalize=0):
+def oracle_sample_step(w, seed=0, expand=1, top_k=1, renormalize=0, expert_choice=0):
     """One bounded CPU-oracle step on the workload: route the whole batch
     (with Expanded Drop over `expand` candidates when > 1, or top-2), then the
     expert FFN and combine of the tokens processed by the first
@@ -177,6 +177,16 @@ def oracle_sample_step(w, seed=0, expand=1, top_k=1, renormalize=0):
     t0 = time.perf_counter()
     r = oracle.route(inp.x, inp.W_g, zipf_bias(w))
     C = oracle.capacity(w.T, w.N, w.capacity_factor)
+    if expert_choice:
+        chosen, gates = oracle.expert_choice(r["probs"], C)
+        slots = 0
+        for e in experts:
+            oracle.forward_rows_expert_choice(chosen[e], inp.x, chosen[e:e + 1], gates[e:e + 1],
+                                              w.gate_multiply, lambda i: experts[e])
+            slots += chosen.shape[1]
+        oracle.aux_loss(r["probs"], np.bincount(r["expert_id"], minlength=w.N))
+        # a token holds N * k / T slots on average
+        return slots * w.T / (w.N * chosen.shape[1]), time.perf_counter() - t0
     if top_k == 2:
         c = oracle.candidates(r["logits"], 2)
         g2 = oracle.top2_gates(r["probs"], c, renormalize)
@@ -225,12 +235,13 @@ def run_reference(args, rank, world):
         w = w.replace(priority_mode=0)
     if rank != 0:
         return
+    kw = dict(expand=args.expand, top_k=args.top_k, renormalize=args.renormalize,
+              expert_choice=args.expert_choice)
     for _ in range(args.warmup):
-        oracle_sample_step(w, expand=args.expand, top_k=args.top_k, renormalize=args.renormalize)
+        oracle_sample_step(w, **kw)
     tok, sec = 0, 0.0
     for _ in range(args.steps):
-        n, s = oracle_sample_step(w, expand=args.expand, top_k=args.top_k,
-                                  renormalize=args.renormalize)
+        n, s = oracle_sample_step(w, **kw)
         tok += n
         sec += s
     value = tok / sec
@@ -240,7 +251,8 @@ def run_reference(args, rank, world):
         "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sec / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(w, args.expand, args.top_k, args.renormalize),
+        "config": workload_config(w, args.expand, args.top_k, args.renormalize,
+                                  args.expert_choice),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": cpu_sample_desc(w)},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -249,14 +261,16 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def workload_config(w, expand=1, top_k=1, renormalize=0):
+def workload_config(w, expand=1, top_k=1, renormalize=0, expert_choice=0):
     route = ("top-2" + (" (gates renormalised over the pair)" if renormalize else "")
              if top_k == 2 else "Switch top-1")
+    if expert_choice:
+        route = "expert-choice"
     return {"workload": f"{w.name}: {route} MoE layer T={w.T} d_model={w.d_model} "
                         f"d_ff={w.d_ff} N={w.N} cf={w.capacity_factor} {w.dtype}"
                         f"{' +shared expert' if w.has_shared else ''}"
                         f"{f' +Expanded Drop over {expand} candidates' if expand > 1 else ''}",
-            "expanded_drop_candidates": expand, "top_k": top_k,
+            "expanded_drop_candidates": expand, "top_k": top_k, "expert_choice": expert_choice,
             "T": w.T, "d_model": w.d_model, "d_ff": w.d_ff, "N": w.N,
             "capacity_factor": w.capacity_factor,
             "priority": "gate" if w.priority_mode else "token-order",
@@ -281,6 +295,8 @@ def main():
                     help="experts per token (2: top-2 token choice)")
     ap.add_argument("--renormalize", type=int, default=0, choices=[0, 1],
                     help="top-2 gates renormalised over the chosen pair")
+    ap.add_argument("--expert-choice", type=int, default=0, choices=[0, 1],
+                    help="expert-choice routing (each expert takes its C best tokens)")
     ap.add_argument("--token-order", action="store_true",
                     help="token-order priority whatever the workload's (Expanded Drop "
                          "on the skewed shape)")
@@ -309,13 +325,19 @@ def main():
     inp = make_inputs(w, seed=0, device=dev)
     p = sm.make_params(w.T, w.d_model, w.d_ff, w.N, w.capacity_factor, w.priority_mode,
                        w.gate_multiply, sm.BF16 if w.dtype == "bf16" else sm.F32, w.has_shared,
-                       args.expand, args.top_k, args.renormalize)
+                       args.expand, args.top_k, args.renormalize, args.expert_choice)
     ws = sm.workspace(sm.switch_moe_workspace_bytes(p), dev)
     out = None
     stream = torch.cuda.current_stream(dev)
 
     def step():
         nonlocal out
+        if args.expert_choice:
+            out = sm.switch_moe_forward_expert_choice(inp.x, inp.W_g, inp.W1, inp.W2,
+                                                      w.capacity_factor, w.gate_multiply,
+                                                      b_g=inp.b_g, W1s=inp.W1s, W2s=inp.W2s,
+                                                      ws=ws, out=out)
+            return
         out = sm.switch_moe_forward(inp.x, inp.W_g, inp.W1, inp.W2, w.capacity_factor,
                                     w.priority_mode, w.gate_multiply, b_g=inp.b_g,
                                     W1s=inp.W1s, W2s=inp.W2s, ws=ws, out=out,
@@ -371,11 +393,18 @@ def main():
     C = sm.switch_moe_capacity(w.T, w.N, w.capacity_factor)
     # filled slots per expert (with Expanded Drop, re-routed tokens count
     # for the expert that runs them)
-    eid, slt = out.expert_id.cpu().numpy(), out.slot.cpu().numpy()
-    kept = np.bincount(eid[slt >= 0], minlength=w.N).astype(np.int64)
+    if args.expert_choice:
+        ch = out.chosen_token.cpu().numpy()
+        kept = (ch >= 0).sum(axis=1).astype(np.int64)
+        out_rows = int((out.experts_per_token.cpu().numpy() > 0).sum())   # y rows written
+        n_choices = w.T   # "dropped" below: tokens no expert took
+    else:
+        eid, slt = out.expert_id.cpu().numpy(), out.slot.cpu().numpy()
+        kept = np.bincount(eid[slt >= 0], minlength=w.N).astype(np.int64)
+        out_rows = int((slt.reshape(w.T, -1) >= 0).any(axis=1).sum())   # y rows written
+        n_choices = w.T * args.top_k
     active = int((kept > 0).sum())
     T_kept = int(kept.sum())   # filled slots (top-2: token-choice pairs)
-    out_rows = int((slt.reshape(w.T, -1) >= 0).any(axis=1).sum())   # y rows written
     eb = 2 if w.dtype == "bf16" else 4
     d, F = w.d_model, w.d_ff
     wbytes_expert = d * F * eb
@@ -407,7 +436,7 @@ def main():
 
     # ---- end to end through the host-buffer entry point
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.expert_choice:   # the host-buffer entry point is top-k only
         x_host = inp.x.cpu().pin_memory()
         hout = None
         hws = sm.workspace(sm.switch_moe_hostio_workspace_bytes(p), dev)
@@ -445,7 +474,8 @@ def main():
         tok, sec = 0, 0.0
         while sec < 10.0:
             n, s = oracle_sample_step(w, expand=args.expand, top_k=args.top_k,
-                                      renormalize=args.renormalize)
+                                      renormalize=args.renormalize,
+                                      expert_choice=args.expert_choice)
             tok += n
             sec += s
         cpu = {"value": tok / sec, "unit": "tokens/s", "cores": blas_threads(),
@@ -457,7 +487,8 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": workload_config(w, args.expand, args.top_k, args.renormalize),
+            "config": workload_config(w, args.expand, args.top_k, args.renormalize,
+                                      args.expert_choice),
             "e2e": e2e,
             "roofline": {"kernel": ("ffn_tc_kernel (expert GEMM 1 + 2, one launch)" if ffn_one
                                     else "gemm_tc_kernel (expert GEMM 1 + 2)"),
@@ -467,7 +498,7 @@ def main():
                          # the ncu figure is for the plain top-1 workload only
                          "traffic": (kernel_traffic(args.config)
                                      if ffn_one and args.expand == 1 and args.top_k == 1
-                                     else None),
+                                     and not args.expert_choice else None),
                          "algorithmic_bytes_per_launch": ffn_bytes},
             "layer_roofline": {"t_roof_us": t_roof * 1e6, "t_step_us": 1e3 * ms / args.steps,
                                "frac": t_roof / (ms / args.steps / 1e3),
@@ -477,7 +508,9 @@ def main():
             "phase_us": {k: 1e3 * v for k, v in phase_ms.items()},
             "routing": {"active_experts": active,
                         # top-2: token-choice pairs kept and dropped
-                        "kept_tokens": T_kept, "dropped": int(w.T * args.top_k - T_kept),
+                        "kept_tokens": T_kept,
+                        "dropped": (int(w.T - out_rows) if args.expert_choice
+                                    else int(n_choices - T_kept)),
                         "capacity": C,
                         "aux_loss": float(out.aux_loss.item())},
             "cpu_baseline": cpu,

@@ -131,6 +131,11 @@ typedef struct switch_moe_params {
    * the two chosen logits, p_e / (p_e0 + p_e1) ([CMP] routing table,
    * Mixtral: softmax over the top-k). */
   int32_t renormalize;
+  /* 1 = expert-choice routing, used only by switch_moe_forward_expert_choice()
+   * and switch_moe_route_expert_choice() (the token-choice entry points
+   * return SWITCH_MOE_ERR_INVALID_ARG for it); 0 otherwise.  Needs top_k <= 1,
+   * expand <= 1 and min(C, T) <= 16384 (SWITCH_MOE_ERR_UNSUPPORTED). */
+  int32_t expert_choice;
 } switch_moe_params;
 
 /* Expert capacity C = ceil(cf * T / N), evaluated in double as (cf*T)/N.
@@ -205,6 +210,47 @@ int switch_moe_route_from_logits_noalloc(const switch_moe_params* p, const float
                                          int32_t* expert_id, float* gate, int32_t* slot,
                                          uint8_t* drop_mask, int32_t* expert_counts,
                                          float* aux_loss, switch_moe_stream_t stream);
+
+/* Expert-choice routing ([TOP1] routing-paradigm table: each expert selects
+ * its top-K tokens; milestone table: Expert Choice Routing, Zhou et al.;
+ * comparison table: a token can be taken by several experts or by none).
+ * p->expert_choice must be 1.  The scores are the top-1 layer's router,
+ * s[t, e] = softmax over the N experts of token t's fp32 logits.  Each
+ * expert takes k = min(C, T) tokens, C = ceil(cf * T / N): those with the
+ * highest s[:, e], the lower token index first among equal scores; slot =
+ * rank.  y[t] = sum over the experts that took t of g * E_e(x_t), g = s[t, e]
+ * (1 when gate_multiply is 0), plus the shared expert; 0 when no expert
+ * took t.  (The pages print no formula for expert choice; this is the
+ * plainest reading of the tables.)
+ * Outputs: y                 [T, d_model] fp32
+ *          chosen_token      [N, C] int32: expert e's tokens, best first; -1 past T
+ *          chosen_gate       [N, C] fp32: their scores s[t, e]; 0 past T
+ *          experts_per_token [T] int32: how many experts took each token
+ *          expert_counts     [N] int32 and aux_loss [1]: the router's top-1
+ *                            statistics (counts of argmax and L_aux, as in
+ *                            switch_moe_forward; expert choice itself needs no
+ *                            balancing loss)
+ * The adds of several slots into a y row are atomic: their order, and so the
+ * last bit of y, can differ between runs.  Workspace, alignment and errors as
+ * for switch_moe_forward(). */
+int switch_moe_forward_expert_choice(const switch_moe_params* p,
+                                     const void* x, const float* W_g, const float* b_g,
+                                     const void* W1, const void* W2,
+                                     const void* W1s, const void* W2s,
+                                     float* y, int32_t* chosen_token, float* chosen_gate,
+                                     int32_t* experts_per_token, int32_t* expert_counts,
+                                     float* aux_loss, void* workspace, size_t workspace_bytes,
+                                     switch_moe_stream_t stream);
+
+/* The routing of switch_moe_forward_expert_choice() on given fp32 logits
+ * [T, N]: the same outputs without y.  Workspace: switch_moe_workspace_bytes()
+ * of a params struct with the same T, N and cf, expert_choice = 1 and
+ * d_model = d_ff = 8. */
+int switch_moe_route_expert_choice(const switch_moe_params* p, const float* logits,
+                                   int32_t* chosen_token, float* chosen_gate,
+                                   int32_t* experts_per_token, int32_t* expert_counts,
+                                   float* aux_loss, void* workspace, size_t workspace_bytes,
+                                   switch_moe_stream_t stream);
 
 /* Step 1 alone: logits [T, N] fp32 = x W_g^T (+ b_g), computed by the same
  * device code that switch_moe_forward() fuses with steps 2-4, so feeding

@@ -12,6 +12,8 @@ Functions carry the C ABI's names:
 
     switch_moe_forward(x, W_g, W1, W2, capacity_factor, ...) -> ForwardOut
     switch_moe_route_from_logits(logits, capacity_factor, ...) -> RouteOut
+    switch_moe_forward_expert_choice(x, W_g, W1, W2, capacity_factor, ...) -> ExpertChoiceOut
+    switch_moe_route_expert_choice(logits, capacity_factor) -> ExpertChoiceOut (y None)
     switch_moe_router_logits(x, W_g, b_g=None) -> logits [T, N] fp32
     switch_moe_forward_hostio(x_host, W_g, W1, W2, ...) -> ForwardOut (host tensors)
     switch_moe_capacity(T, N, cf) -> int
@@ -48,7 +50,8 @@ EXPORTED = (
     "switch_moe_hostio_workspace_bytes", "switch_moe_forward_hostio",
     "switch_moe_sync_status", "switch_moe_strerror", "switch_moe_version",
     "switch_moe_selftest_wait_timeout", "switch_moe_set_phase_events",
-    "switch_moe_route_from_logits_noalloc",
+    "switch_moe_route_from_logits_noalloc", "switch_moe_forward_expert_choice",
+    "switch_moe_route_expert_choice",
 )
 NUM_PHASE_EVENTS = 8
 PHASES = ("router", "scan_aux", "slots_dispatch", "shared_gemms", "expert_gemm1",
@@ -63,7 +66,7 @@ class Params(ctypes.Structure):
         ("priority_mode", ctypes.c_int32), ("gate_multiply", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("has_shared", ctypes.c_int32),
         ("expand", ctypes.c_int32), ("top_k", ctypes.c_int32),
-        ("renormalize", ctypes.c_int32),
+        ("renormalize", ctypes.c_int32), ("expert_choice", ctypes.c_int32),
     ]
 
 
@@ -89,6 +92,11 @@ def _load() -> ctypes.CDLL:
     fwd = [P, V, V, V, V, V, V, V, V, V, V, V, V, V, V, V, ctypes.c_size_t, V]
     lib.switch_moe_forward.argtypes = fwd
     lib.switch_moe_forward.restype = I32
+    # p, 7 inputs, 6 outputs, workspace, its size, stream
+    lib.switch_moe_forward_expert_choice.argtypes = [P] + [V] * 14 + [ctypes.c_size_t, V]
+    lib.switch_moe_forward_expert_choice.restype = I32
+    lib.switch_moe_route_expert_choice.argtypes = [P, V, V, V, V, V, V, V, ctypes.c_size_t, V]
+    lib.switch_moe_route_expert_choice.restype = I32
     lib.switch_moe_forward_hostio.argtypes = fwd
     lib.switch_moe_forward_hostio.restype = I32
     lib.switch_moe_route_from_logits.argtypes = [P, V, V, V, V, V, V, V, V, ctypes.c_size_t, V]
@@ -140,6 +148,15 @@ class ForwardOut(NamedTuple):
     aux_loss: torch.Tensor       # [1] fp32
 
 
+class ExpertChoiceOut(NamedTuple):
+    y: Optional[torch.Tensor]    # [T, d_model] fp32 (None from the routing-only call)
+    chosen_token: torch.Tensor   # [N, C] int32: each expert's tokens, best first; -1 past T
+    chosen_gate: torch.Tensor    # [N, C] fp32: their scores
+    experts_per_token: torch.Tensor  # [T] int32
+    expert_counts: torch.Tensor  # [N] int32: the router's top-1 counts
+    aux_loss: torch.Tensor       # [1] fp32: L_aux of the router's top-1 choice
+
+
 class RouteOut(NamedTuple):
     expert_id: torch.Tensor
     gate: torch.Tensor
@@ -183,10 +200,10 @@ def switch_moe_capacity(T: int, N: int, capacity_factor: float) -> int:
 
 def make_params(T, d_model, d_ff, N, capacity_factor, priority_mode=TOKEN_ORDER,
                 gate_multiply=1, dtype=BF16, has_shared=0, expand=1, top_k=1,
-                renormalize=0) -> Params:
+                renormalize=0, expert_choice=0) -> Params:
     return Params(int(T), int(d_model), int(d_ff), int(N), float(capacity_factor),
                   int(priority_mode), int(gate_multiply), int(dtype), int(has_shared),
-                  int(expand), int(top_k), int(renormalize))
+                  int(expand), int(top_k), int(renormalize), int(expert_choice))
 
 
 def _token_shape(T: int, top_k: int) -> tuple:
@@ -402,6 +419,71 @@ def switch_moe_route_from_logits_noalloc(logits: torch.Tensor, capacity_factor: 
             _ptr(out.drop_mask), _ptr(out.expert_counts), _ptr(out.aux_loss), _stream(stream))
     _check(rc, "switch_moe_route_from_logits_noalloc")
     return out
+
+
+def _ec_outputs(T: int, d: Optional[int], N: int, C: int, dev) -> ExpertChoiceOut:
+    return ExpertChoiceOut(
+        None if d is None else torch.empty((T, d), dtype=torch.float32, device=dev),
+        torch.empty((N, C), dtype=torch.int32, device=dev),
+        torch.empty((N, C), dtype=torch.float32, device=dev),
+        torch.empty(T, dtype=torch.int32, device=dev),
+        torch.empty(N, dtype=torch.int32, device=dev),
+        torch.empty(1, dtype=torch.float32, device=dev))
+
+
+def switch_moe_forward_expert_choice(x: torch.Tensor, W_g: torch.Tensor, W1: torch.Tensor,
+                                     W2: torch.Tensor, capacity_factor: float,
+                                     gate_multiply: int = 1, b_g: Optional[torch.Tensor] = None,
+                                     W1s: Optional[torch.Tensor] = None,
+                                     W2s: Optional[torch.Tensor] = None,
+                                     ws: Optional[torch.Tensor] = None,
+                                     out: Optional[ExpertChoiceOut] = None,
+                                     stream=None) -> ExpertChoiceOut:
+    """The layer with expert-choice routing; see switch_moe_forward_expert_choice
+    in include/switch_moe.h."""
+    dev = x.device
+    _contig(x, "x", None, dev)
+    T, d, F, N = _layer_args(x, W_g, W1, W2, b_g, W1s, W2s, dev)
+    p = make_params(T, d, F, N, capacity_factor, TOKEN_ORDER, gate_multiply, _dtype_code(x),
+                    int(W1s is not None), expert_choice=1)
+    if ws is None:
+        ws = workspace(switch_moe_workspace_bytes(p), dev)
+    C = switch_moe_capacity(T, N, capacity_factor) if T else 0
+    if out is None:
+        out = _ec_outputs(T, d, N, C, dev)
+    want = (T * d, N * C, N * C, T, N, 1)
+    for t, n, name in zip(out, want, ExpertChoiceOut._fields):
+        if t.numel() != n or not t.is_contiguous():
+            raise ValueError(f"out.{name} must be contiguous with {n} elements")
+    with torch.cuda.device(dev):
+        rc = _lib.switch_moe_forward_expert_choice(
+            ctypes.byref(p), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(W1), _ptr(W2), _ptr(W1s),
+            _ptr(W2s), _ptr(out.y), _ptr(out.chosen_token), _ptr(out.chosen_gate),
+            _ptr(out.experts_per_token), _ptr(out.expert_counts), _ptr(out.aux_loss), _ptr(ws),
+            ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check(rc, "switch_moe_forward_expert_choice")
+    return out
+
+
+def switch_moe_route_expert_choice(logits: torch.Tensor, capacity_factor: float,
+                                   ws: Optional[torch.Tensor] = None,
+                                   stream=None) -> ExpertChoiceOut:
+    """Expert-choice routing on given fp32 logits [T, N] (y is None)."""
+    dev = logits.device
+    _contig(logits, "logits", torch.float32)
+    T, N = logits.shape
+    p = make_params(T, 8, 8, N, capacity_factor, TOKEN_ORDER, 1, F32, 0, expert_choice=1)
+    if ws is None:
+        ws = workspace(switch_moe_workspace_bytes(p), dev)
+    C = switch_moe_capacity(T, N, capacity_factor) if T else 0
+    o = _ec_outputs(T, None, N, C, dev)
+    with torch.cuda.device(dev):
+        rc = _lib.switch_moe_route_expert_choice(
+            ctypes.byref(p), _ptr(logits), _ptr(o.chosen_token), _ptr(o.chosen_gate),
+            _ptr(o.experts_per_token), _ptr(o.expert_counts), _ptr(o.aux_loss), _ptr(ws),
+            ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check(rc, "switch_moe_route_expert_choice")
+    return o
 
 
 def switch_moe_router_logits(x: torch.Tensor, W_g: torch.Tensor,

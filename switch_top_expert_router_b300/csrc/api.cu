@@ -98,6 +98,8 @@ struct Plan {
   int expand;        // Expanded Drop candidates (1 = plain top-1)
   int topk;          // experts per token: 1, or 2 (top-2 token choice)
   int renorm;        // top-2 gates renormalised over the pair
+  bool ec;           // expert-choice routing
+  bool multi;        // several slots may add into one y row (top-2, expert choice)
   int elem;          // bytes per x/W element
   int BN, BNs;       // token tiles: routed experts, shared expert
   int max_entries;   // N * ceil(C / BN)
@@ -109,6 +111,7 @@ struct Plan {
   bool tc_router;    // bf16 x and N <= kMaxExpertsTc: tensor-core router
   size_t o_cand, o_candp, o_used;   // Expanded Drop and top-2
   size_t o_hist2, o_rank2, o_cnt2, o_e1, o_g1;   // top-2
+  size_t o_probt, o_sgate;                        // expert choice; slot gates
   size_t o_Ppart, o_hist, o_rank, o_Psum, o_start, o_list, o_entries, o_ctrl, o_wsplit, o_xbuf,
       o_H0, o_H1, o_O, o_Hs0, o_Hs1, o_Os, o_tok, o_part, o_splitcnt, total;
   // extra for the host-IO entry point
@@ -150,6 +153,8 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   if (p->renormalize && p->top_k != 2) return SWITCH_MOE_ERR_INVALID_ARG;
   if (p->top_k == 2 && (p->priority_mode != SWITCH_MOE_TOKEN_ORDER || p->expand > 1 || p->N < 2))
     return SWITCH_MOE_ERR_UNSUPPORTED;
+  if (p->expert_choice != 0 && p->expert_choice != 1) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (p->expert_choice && (p->top_k > 1 || p->expand > 1)) return SWITCH_MOE_ERR_UNSUPPORTED;
   if (need_gemm && (p->d_model < 8 || p->d_ff < 8 || p->d_model % 8 || p->d_ff % 8))
     return SWITCH_MOE_ERR_UNSUPPORTED;
   if (p->T > (int64_t)1 << 30 || p->d_model > (1 << 20) || p->d_ff > (1 << 20))
@@ -163,11 +168,13 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   q.expand = p->expand > 1 ? p->expand : 1;
   q.topk = p->top_k == 2 ? 2 : 1;
   q.renorm = p->renormalize;
+  q.ec = p->expert_choice == 1;
+  q.multi = q.topk == 2 || q.ec;
   if (q.T == 0) return SWITCH_MOE_OK;
   const int64_t C = capacity_of(q.T, q.N, p->capacity_factor);
   if (C < 1) return SWITCH_MOE_ERR_INVALID_ARG;
   if (q.N * C > ((int64_t)1 << 30)) return SWITCH_MOE_ERR_UNSUPPORTED;
-  if (q.mode == SWITCH_MOE_GATE_PRIORITY && (C < q.T ? C : q.T) > kGateSortMax)
+  if ((q.mode == SWITCH_MOE_GATE_PRIORITY || q.ec) && (C < q.T ? C : q.T) > kGateSortMax)
     return SWITCH_MOE_ERR_UNSUPPORTED;
   q.C = (int)C;
   q.R = (int)cdiv(q.T, kRouterTM);
@@ -198,7 +205,13 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   if (q.expand > 1 || q.topk == 2) {
     q.o_cand = take((size_t)q.T * kMaxCand * 4);
     q.o_candp = take((size_t)q.T * kMaxCand * 4);
-    q.o_used = take((size_t)q.N * 4);   // filled slots after the last pass / both choices
+  }
+  if (q.expand > 1 || q.multi)
+    q.o_used = take((size_t)q.N * 4);   // filled slots per expert (passes, choices, selection)
+  if (q.ec) {
+    q.o_probt = take((size_t)q.N * q.T * 4);
+    q.o_e1 = take((size_t)q.T * 4);   // the router's top-1 outputs (statistics only)
+    q.o_g1 = take((size_t)q.T * 4);
   }
   if (q.topk == 2) {
     q.o_hist2 = take((size_t)q.R * q.N * 4);
@@ -218,9 +231,9 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
       q.o_H0 = take((size_t)NC * q.F * 4);
     }
     q.fused = q.bf16 && q.ksplit == 1;
-    if (q.fused) {
-      q.o_tok = take((size_t)NC * 4);
-    } else {
+    if (q.fused || q.ec) q.o_tok = take((size_t)NC * 4);
+    if (q.multi) q.o_sgate = take((size_t)NC * 4);
+    if (!q.fused) {
       q.o_O = take((size_t)q.ksplit * NC * q.d * 4);
     }
     q.ffn = q.fused && q.BN <= 128;
@@ -353,6 +366,7 @@ int run_routing(const Plan& q, const void* x, const float* W_g, const float* b_g
     aa.cand = ra.cand; aa.cand_p = ra.cand_p;
     aa.bases2 = ra.hist2; aa.local_rank2 = ra.local_rank2;
     aa.eid_out = expert_id; aa.gate_out = gate;
+    aa.slot_gate = aa.tok_of_slot ? at<float>(ws, q.o_sgate) : nullptr;
   }
   // with Expanded Drop the work list waits for the last pass (launch_expand)
   const bool finish_here = sa.defer_finish && q.expand == 1;
@@ -409,7 +423,8 @@ int run_gemm(const Plan& q, const DeviceInfo* dev, bool dense, int layer, const 
     g.gate_multiply = q.gm;
     // top-2: two choices add into a row (zeroed, or holding the shared
     // expert's output); top-1: the shared expert's output is already in y
-    g.y_acc = q.topk == 2 ? 2 : q.shared;
+    g.y_acc = q.multi ? 2 : q.shared;
+    g.slot_gate = q.multi ? at<float>(ws, q.o_sgate) : nullptr;
   }
   if (!dense && q.part_units) {
     g.part = at<float>(ws, q.o_part);
@@ -482,7 +497,8 @@ int run_ffn(const Plan& q, const DeviceInfo* dev, const void* W1, const void* W2
   a.H0 = at<__nv_bfloat16>(ws, q.o_H0); a.H1 = at<__nv_bfloat16>(ws, q.o_H1);
   a.y = y; a.tok_of_slot = at<int32_t>(ws, q.o_tok); a.gate = gate;
   a.gate_multiply = q.gm;
-  a.y_acc = q.topk == 2 ? 2 : q.shared;
+  a.y_acc = q.multi ? 2 : q.shared;
+  a.slot_gate = q.multi ? at<float>(ws, q.o_sgate) : nullptr;
   a.part = at<float>(ws, q.o_part); a.part_units = q.part_units;
   a.split_cnt = at<int32_t>(ws, q.o_splitcnt);
   a.stages = ffn_tc_stages(q.BN);
@@ -500,16 +516,71 @@ int run_ffn(const Plan& q, const DeviceInfo* dev, const void* W1, const void* W2
   return SWITCH_MOE_OK;
 }
 
-int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const float* W_g,
-                   const float* b_g, const void* W1, const void* W2, const void* W1s,
-                   const void* W2s, float* y, int32_t* expert_id, float* gate, int32_t* slot,
-                   uint8_t* drop, int32_t* counts, float* aux, void* ws, cudaStream_t s) {
-  int rc = run_routing(q, x, W_g, b_g, nullptr, expert_id, gate, slot, drop, counts, aux, ws,
-                       true, y, dev->status, s);
-  if (rc) return rc;
-  // filled slots per expert: min(counts, C), or after Expanded Drop its
-  // passes' total, or with top-2 both choices' total
-  const int32_t* kept = (q.expand > 1 || q.topk == 2) ? at<int32_t>(ws, q.o_used) : counts;
+// Expert-choice routing: router (+ transposed probabilities) -> scan (top-1
+// statistics, zeroed per-token counts) -> per-expert selection and dispatch
+// (+ work list in an extra CTA).  x == nullptr routes `logits`.
+int run_routing_ec(const Plan& q, const void* x, const float* W_g, const float* b_g,
+                   const float* logits, int32_t* chosen_token, float* chosen_gate,
+                   int32_t* per_token, int32_t* counts, float* aux, void* ws, bool dispatch,
+                   float* y, int* status, cudaStream_t s) {
+  int32_t* ctrl = at<int32_t>(ws, q.o_ctrl);
+  RouterArgs ra{};
+  ra.x = x; ra.W_g = W_g; ra.b_g = b_g; ra.logits_in = logits;
+  ra.T = (int)q.T; ra.d = (int)q.d; ra.N = (int)q.N; ra.x_is_bf16 = q.bf16;
+  ra.expert_id = at<int32_t>(ws, q.o_e1); ra.gate = at<float>(ws, q.o_g1);
+  ra.P_part = at<float>(ws, q.o_Ppart); ra.hist = at<int32_t>(ws, q.o_hist);
+  ra.local_rank = at<int32_t>(ws, q.o_rank); ra.ctrl = ctrl;
+  ra.n_cand = 1;
+  ra.probs_t = at<float>(ws, q.o_probt);
+  mark(0, s);
+  if (x && q.tc_router) {
+    int rc = launch_tc_router(q, ra, ws, status, s);
+    if (rc) return rc;
+  } else if (launch_router(ra, s) != cudaSuccess) {
+    return SWITCH_MOE_ERR_CUDA;
+  }
+  mark(1, s);
+  ScanArgs sa{};
+  sa.hist = ra.hist; sa.P_part = ra.P_part; sa.R = q.R; sa.N = (int)q.N; sa.T = (int)q.T;
+  sa.C = q.C; sa.counts = counts; sa.P_sum = at<float>(ws, q.o_Psum);
+  sa.expert_start = at<int32_t>(ws, q.o_start); sa.aux_loss = aux;
+  sa.entries = at<int2>(ws, q.o_entries); sa.BN = q.BN; sa.ctrl = ctrl;
+  sa.defer_finish = 1;   // the selection kernel's extra CTA runs finish_experts
+  if (dispatch && q.part_units) {
+    sa.split_cnt = at<int32_t>(ws, q.o_splitcnt);
+    sa.n_split_cnt = 4 * q.part_units + q.max_entries + 1;
+  }
+  sa.kept_all = (int)(q.C < q.T ? q.C : q.T);
+  sa.kept_out = at<int32_t>(ws, q.o_used);
+  sa.zero_buf = per_token;
+  sa.n_zero = (int)q.T;
+  if (launch_scan(sa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  mark(2, s);
+  ExpertChoiceArgs ea{};
+  ea.T = (int)q.T; ea.N = (int)q.N; ea.C = q.C; ea.d = (int)q.d; ea.elem_bytes = q.elem;
+  ea.probs_t = ra.probs_t; ea.chosen_token = chosen_token; ea.chosen_gate = chosen_gate;
+  ea.per_token = per_token;
+  if (dispatch) {
+    ea.tok_of_slot = at<int32_t>(ws, q.o_tok);
+    ea.slot_gate = at<float>(ws, q.o_sgate);
+    ea.x = x; ea.xbuf = at<void>(ws, q.o_xbuf);
+    // every slot of a token adds into y: zero it (unless the shared expert
+    // stores its output there first)
+    ea.y = (q.fused && q.shared) ? nullptr : y;
+  }
+  ea.status = status;
+  if (launch_expert_select(ea, sa, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  mark(3, s);
+  return SWITCH_MOE_OK;
+}
+
+// The shared expert, the routed experts' FFN and the combine, after routing.
+// kept: filled slots per expert (capped at C by the kernels).
+int run_experts(const Plan& q, const DeviceInfo* dev, const void* x, const void* W1,
+                const void* W2, const void* W1s, const void* W2s, float* y,
+                const int32_t* kept, int32_t* expert_id, float* gate, int32_t* slot, void* ws,
+                cudaStream_t s) {
+  int rc;
   void* xbuf = at<void>(ws, q.o_xbuf);
   void* H0 = at<void>(ws, q.o_H0);
   void* H1 = q.bf16 ? at<void>(ws, q.o_H1) : nullptr;
@@ -547,6 +618,18 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
   float* O = at<float>(ws, q.o_O);
   if ((rc = run_gemm(q, dev, false, 2, W2, H0, H1, O, nullptr, kept, gate, ws, s))) return rc;
   mark(6, s);
+  if (q.ec) {
+    SlotCombineArgs sc{};
+    sc.T = (int)q.T; sc.N = (int)q.N; sc.C = q.C; sc.d = (int)q.d;
+    sc.ksplit = q.bf16 ? q.ksplit : 1;
+    sc.kept = (int)(q.C < q.T ? q.C : q.T);
+    sc.gate_multiply = q.gm;
+    sc.tok_of_slot = at<int32_t>(ws, q.o_tok); sc.slot_gate = at<float>(ws, q.o_sgate);
+    sc.O = O; sc.split_stride = (size_t)q.N * q.C * q.d; sc.S = Os; sc.y = y;
+    if (launch_combine_slots(sc, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+    mark(7, s);
+    return SWITCH_MOE_OK;
+  }
   CombineArgs ca{};
   ca.T = (int)q.T; ca.d = (int)q.d; ca.C = q.C;
   ca.ksplit = q.bf16 ? q.ksplit : 1;
@@ -556,6 +639,31 @@ int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const fl
   if (launch_combine(ca, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   mark(7, s);
   return SWITCH_MOE_OK;
+}
+
+int forward_device(const Plan& q, const DeviceInfo* dev, const void* x, const float* W_g,
+                   const float* b_g, const void* W1, const void* W2, const void* W1s,
+                   const void* W2s, float* y, int32_t* expert_id, float* gate, int32_t* slot,
+                   uint8_t* drop, int32_t* counts, float* aux, void* ws, cudaStream_t s) {
+  int rc = run_routing(q, x, W_g, b_g, nullptr, expert_id, gate, slot, drop, counts, aux, ws,
+                       true, y, dev->status, s);
+  if (rc) return rc;
+  // filled slots per expert: min(counts, C), or after Expanded Drop its
+  // passes' total, or with top-2 both choices' total
+  const int32_t* kept = (q.expand > 1 || q.topk == 2) ? at<int32_t>(ws, q.o_used) : counts;
+  return run_experts(q, dev, x, W1, W2, W1s, W2s, y, kept, expert_id, gate, slot, ws, s);
+}
+
+int forward_ec_device(const Plan& q, const DeviceInfo* dev, const void* x, const float* W_g,
+                      const float* b_g, const void* W1, const void* W2, const void* W1s,
+                      const void* W2s, float* y, int32_t* chosen_token, float* chosen_gate,
+                      int32_t* per_token, int32_t* counts, float* aux, void* ws,
+                      cudaStream_t s) {
+  int rc = run_routing_ec(q, x, W_g, b_g, nullptr, chosen_token, chosen_gate, per_token, counts,
+                          aux, ws, true, y, dev->status, s);
+  if (rc) return rc;
+  return run_experts(q, dev, x, W1, W2, W1s, W2s, y, at<int32_t>(ws, q.o_used), nullptr,
+                     nullptr, nullptr, ws, s);
 }
 
 int empty_batch(int32_t* counts, float* aux, int64_t N, cudaStream_t s) {
@@ -608,7 +716,7 @@ int switch_moe_forward(const switch_moe_params* p, const void* x, const float* W
   Plan q;
   int rc = make_plan(p, &q, true);
   if (rc) return rc;
-  if (!expert_counts || !aux_loss) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (q.ec || !expert_counts || !aux_loss) return SWITCH_MOE_ERR_INVALID_ARG;
   const DeviceInfo* dev = current_device();
   if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -635,6 +743,7 @@ int switch_moe_forward_hostio(const switch_moe_params* p, const void* x_host, co
   Plan q;
   int rc = make_plan(p, &q, true);
   if (rc) return rc;
+  if (q.ec) return SWITCH_MOE_ERR_INVALID_ARG;   // switch_moe_forward_expert_choice
   const DeviceInfo* dev = current_device();
   if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
   if (!x_host || !W_g || !W1 || !W2 || !y_host || !expert_id_host || !gate_host || !slot_host ||
@@ -694,7 +803,7 @@ int switch_moe_route_from_logits(const switch_moe_params* p, const float* logits
   Plan q;
   int rc = make_plan(&pr, &q, false);
   if (rc) return rc;
-  if (!expert_counts || !aux_loss) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (q.ec || !expert_counts || !aux_loss) return SWITCH_MOE_ERR_INVALID_ARG;
   const DeviceInfo* dev = current_device();
   if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -709,6 +818,68 @@ int switch_moe_route_from_logits(const switch_moe_params* p, const float* logits
   t_phase_on = false;   // phase events belong to the forward calls only
   rc = run_routing(q, nullptr, nullptr, nullptr, logits, expert_id, gate, slot, drop_mask,
                    expert_counts, aux_loss, workspace, false, nullptr, dev->status, s);
+  t_phase_on = on;
+  return rc;
+}
+
+int switch_moe_forward_expert_choice(const switch_moe_params* p, const void* x, const float* W_g,
+                                     const float* b_g, const void* W1, const void* W2,
+                                     const void* W1s, const void* W2s, float* y,
+                                     int32_t* chosen_token, float* chosen_gate,
+                                     int32_t* experts_per_token, int32_t* expert_counts,
+                                     float* aux_loss, void* workspace, size_t workspace_bytes,
+                                     switch_moe_stream_t stream) {
+  Plan q;
+  int rc = make_plan(p, &q, true);
+  if (rc) return rc;
+  if (!q.ec || !expert_counts || !aux_loss) return SWITCH_MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = current_device();
+  if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (q.T == 0) return empty_batch(expert_counts, aux_loss, q.N, s);
+  if (!x || !W_g || !W1 || !W2 || !y || !chosen_token || !chosen_gate || !experts_per_token ||
+      !workspace)
+    return SWITCH_MOE_ERR_INVALID_ARG;
+  if (q.shared && (!W1s || !W2s)) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (!al(x, 16) || !al(W_g, 16) || !al(W1, 16) || !al(W2, 16) || !al(y, 16) ||
+      !al(workspace, 256) || !al(chosen_token, 4) || !al(chosen_gate, 4) ||
+      !al(experts_per_token, 4) || !al(expert_counts, 4) || !al(aux_loss, 4) ||
+      (b_g && !al(b_g, 4)) || (q.shared && (!al(W1s, 16) || !al(W2s, 16))))
+    return SWITCH_MOE_ERR_ALIGNMENT;
+  if (workspace_bytes < q.total) return SWITCH_MOE_ERR_WORKSPACE_TOO_SMALL;
+  return forward_ec_device(q, dev, x, W_g, b_g, W1, W2, W1s, W2s, y, chosen_token, chosen_gate,
+                           experts_per_token, expert_counts, aux_loss, workspace, s);
+}
+
+int switch_moe_route_expert_choice(const switch_moe_params* p, const float* logits,
+                                   int32_t* chosen_token, float* chosen_gate,
+                                   int32_t* experts_per_token, int32_t* expert_counts,
+                                   float* aux_loss, void* workspace, size_t workspace_bytes,
+                                   switch_moe_stream_t stream) {
+  if (!p) return SWITCH_MOE_ERR_INVALID_ARG;
+  switch_moe_params pr = *p;
+  pr.d_model = 8;
+  pr.d_ff = 8;
+  pr.has_shared = 0;
+  Plan q;
+  int rc = make_plan(&pr, &q, false);
+  if (rc) return rc;
+  if (!q.ec || !expert_counts || !aux_loss) return SWITCH_MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = current_device();
+  if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (q.T == 0) return empty_batch(expert_counts, aux_loss, q.N, s);
+  if (!logits || !chosen_token || !chosen_gate || !experts_per_token || !workspace)
+    return SWITCH_MOE_ERR_INVALID_ARG;
+  if (!al(logits, 4) || !al(workspace, 256) || !al(chosen_token, 4) || !al(chosen_gate, 4) ||
+      !al(experts_per_token, 4) || !al(expert_counts, 4) || !al(aux_loss, 4))
+    return SWITCH_MOE_ERR_ALIGNMENT;
+  if (workspace_bytes < q.total) return SWITCH_MOE_ERR_WORKSPACE_TOO_SMALL;
+  const bool on = t_phase_on;
+  t_phase_on = false;
+  rc = run_routing_ec(q, nullptr, nullptr, nullptr, logits, chosen_token, chosen_gate,
+                      experts_per_token, expert_counts, aux_loss, workspace, false, nullptr,
+                      dev->status, s);
   t_phase_on = on;
   return rc;
 }

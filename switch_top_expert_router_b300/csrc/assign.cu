@@ -97,10 +97,9 @@ __device__ void finish_experts(const ScanArgs& a, int* sh_i, double* sh_d) {
       const int c = __ldcg(a.counts + i);
       const float p = __ldcg(a.P_sum + i);
       int kept = a.kept ? __ldcg(a.kept + i) : min(c, a.C);
-      if (a.counts2) {   // top-2: first choices, then second choices up to C
-        kept = min(a.C, kept + __ldcg(a.counts2 + i));
-        a.kept_out[i] = kept;
-      }
+      if (a.counts2) kept = min(a.C, kept + __ldcg(a.counts2 + i));   // top-2: then choice 1
+      if (a.kept_all > 0) kept = a.kept_all;                          // expert choice
+      if (a.kept_out) a.kept_out[i] = kept;
       cv[j] = c;
       nv[j] = (kept + a.BN - 1) / a.BN;
       c_loc += c;
@@ -140,6 +139,10 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanArgs a) {
   __shared__ int is_last;
   grid_dep_wait();
   grid_dep_launch();
+  if (a.zero_buf)
+    for (int i = blockIdx.x * kScanThreads + threadIdx.x; i < a.n_zero;
+         i += gridDim.x * kScanThreads)
+      a.zero_buf[i] = 0;
   // CTAs N .. 2N-1 (top-2): the second choices' histograms, no probabilities
   const bool second = blockIdx.x >= a.N;
   const int e = second ? blockIdx.x - a.N : blockIdx.x, tid = threadIdx.x;
@@ -278,8 +281,14 @@ __device__ __forceinline__ void assign_top2(const AssignArgs& a, int t, uint8_t*
     a.drop[2 * (size_t)t] = k0 ? 0 : 1;
     a.drop[2 * (size_t)t + 1] = k1 ? 0 : 1;
     if (a.xbuf && a.tok_of_slot) {
-      if (k0) a.tok_of_slot[(size_t)e0 * a.C + s0] = 2 * t;
-      if (k1) a.tok_of_slot[(size_t)e1 * a.C + s1] = 2 * t + 1;
+      if (k0) {
+        a.tok_of_slot[(size_t)e0 * a.C + s0] = t;
+        a.slot_gate[(size_t)e0 * a.C + s0] = g0;
+      }
+      if (k1) {
+        a.tok_of_slot[(size_t)e1 * a.C + s1] = t;
+        a.slot_gate[(size_t)e1 * a.C + s1] = g1;
+      }
     }
   }
   if (staged) {
@@ -523,6 +532,54 @@ __device__ void bitonic_sort_asc(unsigned long long* k, int P) {
   }
 }
 
+// One radix-select step, run by warp 0: the first digit whose cumulative
+// count over hist[0..255] reaches *krem (255 if none does); *krem drops by
+// the count below it, and the digit joins *prefix / *mask at `shift`.  Each
+// lane scans 8 bins; a warp scan and a ballot find the digit.
+__device__ __forceinline__ void radix_pick(const int* hist, int shift, int* krem,
+                                           unsigned long long* prefix,
+                                           unsigned long long* mask, int* in_bin = nullptr) {
+  const int lane = threadIdx.x & 31;
+  int c[8], tot = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    c[j] = hist[lane * 8 + j];
+    tot += c[j];
+  }
+  int inc = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += o;
+  }
+  const int need = *krem;
+  int below = inc - tot, dg = -1;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (dg < 0) {
+      if (below + c[j] >= need) {
+        dg = lane * 8 + j;
+      } else {
+        below += c[j];
+      }
+    }
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, dg >= 0);
+  const int src = hit ? __ffs(hit) - 1 : 31;
+  int digit = __shfl_sync(0xffffffffu, dg, src);
+  int under = __shfl_sync(0xffffffffu, below, src);
+  if (!hit) {   // no bin reaches krem: the last digit, everything below it counted
+    digit = 255;
+    under = __shfl_sync(0xffffffffu, inc, 31) - hist[255];
+  }
+  if (lane == 0) {
+    *krem = need - under;
+    *prefix |= (unsigned long long)digit << shift;
+    *mask |= 255ull << shift;
+    if (in_bin) *in_bin = hist[digit];
+  }
+}
+
 __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(AssignArgs a) {
   extern __shared__ unsigned long long sk[];   // [kGateSortMax]
   __shared__ int hist[256];
@@ -561,16 +618,7 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(AssignArgs a) 
       if ((k & msk) == pre) atomicAdd(&hist[(int)((k >> shift) & 255ull)], 1);
     }
     __syncthreads();
-    if (tid == 0) {
-      int cum = 0, dg = 0;
-      for (; dg < 255; ++dg) {
-        if (cum + hist[dg] >= s_krem) break;
-        cum += hist[dg];
-      }
-      s_krem -= cum;
-      s_prefix = pre | ((unsigned long long)dg << shift);
-      s_mask = msk | (255ull << shift);
-    }
+    if (tid < 32) radix_pick(hist, shift, &s_krem, &s_prefix, &s_mask);
     __syncthreads();
   }
   const unsigned long long thr = s_prefix;
@@ -598,6 +646,142 @@ __global__ void __launch_bounds__(kSelThreads) gate_select_kernel(AssignArgs a) 
     const int t = (int)(unsigned)(sk[i] & 0xffffffffull);
     a.slot[t] = i;
     a.drop[t] = 0;
+  }
+}
+
+// ------------------------------------------------------- expert choice
+// Expert choice ("Top-1 路由 (Top-1 Routing)", compassingai.com,
+// routing-paradigm table: each expert selects its top-K tokens; milestone
+// table: Expert Choice Routing): expert e keeps the min(C, T) tokens with
+// the highest router probability s[t, e], the lower token index first
+// among equal scores, slot = rank.  Keys (~bits(s) << 32 | t) order that
+// way (scores are >= 0, so their bit patterns order like their values).
+__device__ __forceinline__ unsigned long long ec_key(const float* col, int t) {
+  return ((unsigned long long)(~__float_as_uint(col[t])) << 32) | (unsigned)t;
+}
+
+__global__ void __launch_bounds__(kSelThreads) expert_select_kernel(ExpertChoiceArgs a,
+                                                                    ScanArgs fin) {
+  extern __shared__ unsigned long long sk[];   // [kGateSortMax]
+  __shared__ int hist[256];
+  __shared__ unsigned long long s_prefix, s_mask;
+  __shared__ int s_krem, s_cnt;
+  __shared__ int sh_i[33];
+  __shared__ double sh_d[32];
+  grid_dep_wait();
+  grid_dep_launch();
+  if (blockIdx.x == gridDim.x - 1) {   // the extra CTA: work list and L_aux
+    finish_experts(fin, sh_i, sh_d);
+    return;
+  }
+  const int e = blockIdx.x, tid = threadIdx.x, T = a.T;
+  const int lane = tid & 31, warp = tid >> 5;
+  const float* col = a.probs_t + (size_t)e * T;
+  const int k = min(a.C, T);
+  if (a.y) {   // rows t = e, e + N, ...: the combine adds every slot of a token into y
+    const int nv = a.d >> 2;
+    const int rows = (T - e + a.N - 1) / a.N;
+    float4* y4 = reinterpret_cast<float4*>(a.y);
+    for (size_t i = tid; i < (size_t)rows * nv; i += kSelThreads) {
+      const size_t t = (size_t)e + (i / nv) * a.N;
+      y4[t * nv + i % nv] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  // keys in shared memory when they fit (T <= kGateSortMax), else re-read
+  const bool cached = T <= kGateSortMax;
+  if (cached)
+    for (int i = tid; i < T; i += kSelThreads) sk[i] = ec_key(col, i);
+  auto key_at = [&](int i) { return cached ? sk[i] : ec_key(col, i); };
+  if (k < T) {
+    // the k-th smallest key by MSB-first radix select (keys are unique);
+    // histogram updates are aggregated per warp (scores share high bits).
+    // The four score digits usually settle it: when the expert keeps every
+    // key of the boundary score, the token digits are not needed.
+    __shared__ int s_inbin;
+    if (tid == 0) { s_prefix = 0ull; s_mask = 0ull; s_krem = k; s_cnt = 0; }
+    __syncthreads();
+    unsigned long long thr = 0ull;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += kSelThreads) hist[i] = 0;
+      __syncthreads();
+      const unsigned long long pre = s_prefix, msk = s_mask;
+      for (int i0 = 0; i0 < T; i0 += kSelThreads) {
+        const int i = i0 + tid;
+        int dg = -1;
+        if (i < T) {
+          const unsigned long long key = key_at(i);
+          if ((key & msk) == pre) dg = (int)((key >> shift) & 255ull);
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, dg);
+        if (dg >= 0 && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(&hist[dg], __popc(peers));
+      }
+      __syncthreads();
+      if (tid < 32) radix_pick(hist, shift, &s_krem, &s_prefix, &s_mask, &s_inbin);
+      __syncthreads();
+      thr = s_prefix;
+      if (shift == 32 && s_krem == s_inbin) {   // all keys of the boundary score stay
+        thr |= 0xffffffffull;
+        break;
+      }
+    }
+    // keys <= thr, compacted in index order (in place when cached: every
+    // thread reads its keys before any is written)
+    constexpr int kPer = kGateSortMax / kSelThreads;
+    unsigned long long mine[kPer];
+    int cnt = 0;
+    if (cached) {
+      unsigned keep = 0;   // bit j: key tid * kPer + j stays
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int i = tid * kPer + j;
+        mine[j] = i < T ? sk[i] : 0ull;
+        if (i < T && mine[j] <= thr) keep |= 1u << j;
+      }
+      cnt = __popc(keep);
+      int total;
+      int pos = block_exclusive_scan(cnt, &total, sh_i);   // synchronises the reads
+#pragma unroll
+      for (int j = 0; j < kPer; ++j)
+        if (keep & (1u << j)) sk[pos++] = mine[j];
+    } else {
+      for (int i = tid; i < T; i += kSelThreads) {
+        const unsigned long long key = ec_key(col, i);
+        if (key <= thr) {
+          const int pos = atomicAdd(&s_cnt, 1);
+          if (pos < kGateSortMax) sk[pos] = key;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  int P = 1;
+  while (P < k) P <<= 1;
+  for (int i = k + tid; i < P; i += kSelThreads) sk[i] = ~0ull;
+  __syncthreads();
+  bitonic_sort_asc(sk, P);
+  const size_t base = (size_t)e * a.C;
+  for (int i = tid; i < a.C; i += kSelThreads) {
+    int t = -1;
+    float g = 0.f;
+    if (i < k) {
+      t = (int)(unsigned)(sk[i] & 0xffffffffull);
+      g = __uint_as_float(~(unsigned)(sk[i] >> 32));
+      atomicAdd(a.per_token + t, 1);
+      if (a.tok_of_slot) {
+        a.tok_of_slot[base + i] = t;
+        a.slot_gate[base + i] = g;
+      }
+    }
+    a.chosen_token[base + i] = t;
+    a.chosen_gate[base + i] = g;
+  }
+  if (a.xbuf) {   // dispatch: one warp per kept row
+    const uint32_t rb = (uint32_t)a.d * (uint32_t)a.elem_bytes;
+    for (int i = warp; i < k; i += kSelThreads / 32) {
+      const int t = (int)(unsigned)(sk[i] & 0xffffffffull);
+      copy_row(static_cast<const char*>(a.x) + (size_t)t * rb,
+               static_cast<char*>(a.xbuf) + (base + i) * rb, (int)rb, lane);
+    }
   }
 }
 
@@ -634,6 +818,15 @@ cudaError_t launch_dispatch(const AssignArgs& a, cudaStream_t s, bool pdl) {
   if (err != cudaSuccess) return err;
   return launch_k(dispatch_kernel, dim3((a.T + kRowWarps - 1) / kRowWarps), dim3(kRowWarps * 32),
                   smem, s, pdl, a);
+}
+
+cudaError_t launch_expert_select(const ExpertChoiceArgs& a, const ScanArgs& fin, cudaStream_t s,
+                                 bool pdl) {
+  const size_t smem = (size_t)kGateSortMax * sizeof(unsigned long long);
+  cudaError_t err = cudaFuncSetAttribute(expert_select_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  return launch_k(expert_select_kernel, dim3(a.N + 1), dim3(kSelThreads), smem, s, pdl, a, fin);
 }
 
 cudaError_t launch_gate_select(const AssignArgs& a, cudaStream_t s, bool pdl) {

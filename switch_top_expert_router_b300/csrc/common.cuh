@@ -64,6 +64,9 @@ struct RouterArgs {
   // second choice cand[1], like hist / local_rank for the first; or null
   int32_t* hist2;         // [R, N]
   int32_t* local_rank2;   // [T]
+  // expert choice: every probability, transposed (expert e's scores of all
+  // tokens contiguous), or null
+  float* probs_t;         // [N, T]
 };
 
 // A token's first kMaxCand experts by logit, descending, lowest index first
@@ -133,6 +136,12 @@ struct ScanArgs {
   int32_t* hist2;
   int32_t* counts2;
   int32_t* kept_out;
+  // expert choice: every expert keeps kept_all tokens (> 0), or 0
+  int kept_all;
+  // zeroed by the scan's CTAs (expert choice: the per-token expert counts
+  // the selection then increments), or null
+  int32_t* zero_buf;
+  int n_zero;
 };
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s, bool pdl = false);
 
@@ -167,6 +176,7 @@ struct AssignArgs {
   const int32_t* local_rank2;  // [T]
   int32_t* eid_out;            // [T, 2]
   float* gate_out;             // [T, 2]
+  float* slot_gate;            // [N * C] gate of each filled slot, for the combine
 };
 // Token order: slot, drop and the dispatch copy in one pass.
 // Gate priority: only the per-expert token lists.
@@ -198,6 +208,27 @@ struct ExpandArgs {
   const void* x;               // null: routing only
   void* xbuf;
 };
+// ------------------------------------------------------- expert choice
+struct ExpertChoiceArgs {
+  int T, N, C, d, elem_bytes;
+  const float* probs_t;        // [N, T] router probabilities, transposed
+  int32_t* chosen_token;       // [N, C] out: each expert's tokens, best first; -1 past T
+  float* chosen_gate;          // [N, C] out: their scores (0 past T)
+  int32_t* per_token;          // [T] out: experts that took each token (zeroed by the scan)
+  int32_t* tok_of_slot;        // [N * C] or null
+  float* slot_gate;            // [N * C] or null
+  const void* x;               // null: routing only
+  void* xbuf;
+  float* y;                    // [T, d]: zeroed for the combine's adds, or null
+  int* status;
+};
+// One CTA per expert: the expert's min(C, T) best tokens by (score desc,
+// token asc) -- radix select of the C-th key, then a sort of the kept keys --
+// their slots, gates and dispatch copies; one extra CTA runs finish_experts
+// (fin.kept_all = min(C, T)).
+cudaError_t launch_expert_select(const ExpertChoiceArgs& a, const ScanArgs& fin, cudaStream_t s,
+                                 bool pdl);
+
 // Passes 2..k in one CTA, after the top-1 pass placed its tokens: the
 // unplaced tokens in token order try their next candidate while it has
 // room; then finish_experts over the final filled slots (fin.kept = used).
@@ -230,9 +261,11 @@ struct GemmArgs {
   const int32_t* tok_of_slot;   // [N * C]
   const float* gate;            // [T]
   int gate_multiply;
-  // 0: store; 1: add to y (one writer per row); 2: top-2, tok_of_slot holds
-  // 2 token + choice and both choices add into y atomically
+  // 0: store; 1: add to y (one writer per row); 2: several slots add into
+  // one row (top-2, expert choice): atomic adds, each slot's gate from
+  // slot_gate
   int y_acc;
+  const float* slot_gate;   // [N * C], y_acc 2
   // Tensor path, ksplit == 1: when the last wave of tiles is less than half
   // full, its tiles are cut along K into pieces that run on the idle CTAs;
   // the pieces leave fp32 partials and the last piece of each 32-row slice
@@ -274,12 +307,14 @@ struct FfnArgs {
   __nv_bfloat16* H0;          // [N * C, F] hi
   __nv_bfloat16* H1;          // [N * C, F] lo
   float* y;                   // [T, d]
-  const int32_t* tok_of_slot; // [N * C] token, or 2 token + choice (y_acc 2); gate index
-  const float* gate;          // [T] or [T, 2]
+  const int32_t* tok_of_slot; // [N * C] token of each filled slot
+  const float* gate;          // [T] (y_acc 0, 1)
   int gate_multiply;
-  // 0: store; 1: add to y (one writer per row); 2: top-2, both choices add
-  // into y atomically
+  // 0: store; 1: add to y (one writer per row); 2: several slots add into
+  // one row (top-2, expert choice): atomic adds, each slot's gate from
+  // slot_gate
   int y_acc;
+  const float* slot_gate;     // [N * C], y_acc 2
   float* part;                // tail split partials [part_units][128 * BN], or null
   int part_units;
   int32_t* split_cnt;         // [4 * part_units]
@@ -308,6 +343,21 @@ struct CombineArgs {
   float* y;                 // [T, d]
 };
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s, bool pdl = false);
+
+// Combine by slots (expert choice on the paths without the fused combine):
+// y[tok(slot)] += g(slot) * sum_k O_k[slot] for every filled slot, and
+// y[t] += S[t] -- atomic adds into a y the selection zeroed.
+struct SlotCombineArgs {
+  int T, N, C, d, ksplit, kept;   // kept: filled slots per expert
+  int gate_multiply;
+  const int32_t* tok_of_slot;     // [N * C]
+  const float* slot_gate;         // [N * C]
+  const float* O;                 // [ksplit][N * C, d]
+  size_t split_stride;
+  const float* S;                 // [T, d] or null
+  float* y;
+};
+cudaError_t launch_combine_slots(const SlotCombineArgs& a, cudaStream_t s, bool pdl = false);
 
 // status word of the current device (see switch_moe_sync_status)
 int* device_status_ptr();

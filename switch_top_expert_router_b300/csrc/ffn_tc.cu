@@ -10,9 +10,9 @@
 // where capacity comes from); GEMM 2's epilogue is the combine step (the
 // gate scales the expert output when gate_multiply is set: the Switch
 // Transformer walk-through's Switch layer, Eq. 2, against Top-1 Routing's
-// step 3).  With top-2 routing a token's two choices add into its y row
-// with atomic adds (the row starts at zero or at the shared expert's
-// output).  Tile shapes, operand layouts, the hi + lo split of H and the
+// step 3).  With top-2 or expert-choice routing several slots of one token
+// add into its y row with atomic adds (the row starts at zero or at the
+// shared expert's output).  Tile shapes, operand layouts, the hi + lo split of H and the
 // epilogues are those of gemm_tc.cu (swap AB: expert weights are the
 // 128-row MMA M, the expert's tokens the MMA N).
 //
@@ -134,8 +134,9 @@ __device__ bool wait_count(const int32_t* cnt, int target, volatile int* abort_f
   return false;
 }
 
-// kAtomicY: top-2, each choice adds into its token's y row atomically
-// (a separate instantiation: the combine loop's code size costs time).
+// kAtomicY: several slots add into one token's y row (top-2, expert
+// choice): atomic adds, gates per slot (a separate instantiation: the
+// combine loop's code size costs time).
 template <bool kAtomicY>
 __global__ void __launch_bounds__(kThreads, 1)
     ffn_tc_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmX,
@@ -412,9 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tk = 0;
         gv = 1.f;
         if (c + lane < u.nv) {
-          const int code = a.tok_of_slot[out_row0 + (size_t)(c + lane)];
-          tk = kAtomicY ? code >> 1 : code;   // token row; code indexes the gate of this choice
-          if (a.gate_multiply) gv = a.gate[code];
+          tk = a.tok_of_slot[out_row0 + (size_t)(c + lane)];
+          if (a.gate_multiply)   // several slots per token: the gate belongs to the slot
+            gv = kAtomicY ? a.slot_gate[out_row0 + (size_t)(c + lane)] : a.gate[tk];
         }
       };
       int tk32 = 0;
@@ -517,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float* dst = a.y + (size_t)tj * (size_t)a.d + row;
               const float val = gj * v[jj >> 4][jj & 15];
               if constexpr (kAtomicY) {
-                atomicAdd(dst, val);   // top-2: two choices add into one row
+                atomicAdd(dst, val);   // several slots add into one row
               } else {
                 *dst = a.y_acc ? *dst + val : val;
               }

@@ -134,8 +134,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
 }
 
 // kEpi: the epilogue (GemmArgs::epi), fixed at compile time so each variant
-// carries only its own store path; 3 is the combine of top-2 routing (slot
-// codes 2 t + choice, atomic adds into y).
+// carries only its own store path; 3 is the combine with several slots per
+// token (top-2, expert choice): gates per slot, atomic adds into y.
 template <int kEpi>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -302,9 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tk = 0;
         gv = 1.f;
         if (c + lane < w.nv) {
-          const int code = g.tok_of_slot[out_row0 + (size_t)(c + lane)];
-          tk = kEpi == 3 ? code >> 1 : code;   // token row; code indexes the gate of this choice
-          if (g.gate_multiply) gv = g.gate[code];
+          tk = g.tok_of_slot[out_row0 + (size_t)(c + lane)];
+          if (g.gate_multiply)   // several slots per token: the gate belongs to the slot
+            gv = kEpi == 3 ? g.slot_gate[out_row0 + (size_t)(c + lane)] : g.gate[tk];
         }
       };
       int tk32 = 0;
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float* dst = y + (size_t)tj * (size_t)g.ldo + row;
               const float val = gj * v[j >> 4][j & 15];
               if constexpr (kEpi == 3) {
-                atomicAdd(dst, val);   // top-2: two choices add into one row
+                atomicAdd(dst, val);   // several slots add into one row
               } else {
                 *dst = g.y_acc ? *dst + val : val;
               }
@@ -456,7 +456,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& g, const CUtensorMap& tmA, const CUte
                            const CUtensorMap& tmB1, cudaStream_t s, bool pdl) {
   auto kern = g.epi == 0   ? gemm_tc_kernel<0>
               : g.epi == 1 ? gemm_tc_kernel<1>
-              : g.y_acc == 2 ? gemm_tc_kernel<3>   // combine with atomic adds (top-2)
+              : g.y_acc == 2 ? gemm_tc_kernel<3>   // combine with atomic adds
                              : gemm_tc_kernel<2>;
   cudaError_t err =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem_bytes);

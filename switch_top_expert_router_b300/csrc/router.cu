@@ -141,7 +141,10 @@ __device__ void route_tile(float* lg, int ldl, int T, int N, int t0, int cta,
   const int nt = min(TM, T - t0);
   for (int i = tid; i < N; i += NTHREADS) {
     float acc = 0.f;
-    for (int r = 0; r < nt; ++r) acc += lg[r * ldl + i];
+    for (int r = 0; r < nt; ++r) {
+      acc += lg[r * ldl + i];
+      if (a.probs_t) a.probs_t[(size_t)i * T + t0 + r] = lg[r * ldl + i];
+    }
     a.P_part[(size_t)cta * N + i] = acc;
   }
   // histogram + rank among earlier same-expert tokens of this CTA (TM == 32)

@@ -149,9 +149,14 @@ __device__ __noinline__ void route_group_smem(const RouterArgs& a, float* lg, fl
   const int g = blockIdx.x * 4 + q;   // 32-token group
   // group sums of p = exp(l - m) / s per expert, tokens in order
   const float* rows = lg + (size_t)q * 32 * kEpiLd;
+  float* pt = a.probs_t;   // expert choice: the probabilities, transposed
   for (int c = lane; c < N; c += 32) {
     float acc = 0.f;
-    for (int rr = 0; rr < nvalid; ++rr) acc += rows[(size_t)rr * kEpiLd + c] * invs[q * 32 + rr];
+    for (int rr = 0; rr < nvalid; ++rr) {
+      const float pv = rows[(size_t)rr * kEpiLd + c] * invs[q * 32 + rr];
+      acc += pv;
+      if (pt) pt[(size_t)c * T + t0 + q * 32 + rr] = pv;
+    }
     a.P_part[(size_t)g * N + c] = acc;
   }
   // histogram and rank among earlier same-expert tokens of the group
@@ -508,7 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (!a.logits_out && group_ok && c0 + lane < N) {
           float acc = 0.f;
-          for (int r = 0; r < 32; ++r) acc += pw[r * 33 + lane];
+          for (int r = 0; r < 32; ++r) {
+            acc += pw[r * 33 + lane];
+            if (a.probs_t && t0 + q * 32 + r < T)
+              a.probs_t[(size_t)(c0 + lane) * T + t0 + q * 32 + r] = pw[r * 33 + lane];
+          }
           a.P_part[(size_t)g * N + c0 + lane] = acc;
         }
         __syncwarp();
