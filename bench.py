@@ -49,8 +49,8 @@ from workloads import CONFIGS, expert_weights, make_inputs, zipf_bias  # noqa: E
 # it was taken on (sha256 of the .cu file); any other source reports null.
 NCU_TRAFFIC = {
     "base": {"source": "ffn_tc.cu",
-             "sha256": "7f6275b361c33e0ae7f077934eab58c3723bdfa7ecf7c2aca7b5b54708f54d44",
-             "bytes_per_launch": (1267.072 + 87.484) * 1e6},
+             "sha256": "a5146f7cec1dc865409a4d5070ad96fceda3457533920cbe7ff528ed7f46dd58",
+             "bytes_per_launch": (1266.141 + 85.651) * 1e6},
 }
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
