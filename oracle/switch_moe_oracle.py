@@ -60,7 +60,7 @@ __all__ = [
     "assign_slots", "expert_ffn", "aux_loss", "combine_token", "forward",
     "forward_rows", "candidates", "assign_slots_expanded", "top2_gates",
     "assign_slots_top2", "forward_top2", "forward_rows_top2", "expert_choice",
-    "forward_expert_choice", "forward_rows_expert_choice",
+    "forward_expert_choice", "forward_rows_expert_choice", "backward",
 ]
 
 TOKEN_ORDER = 0
@@ -463,6 +463,73 @@ def forward_top2(x, W_g, W1, W2, capacity_factor: float, gate_multiply: int = 1,
     return {"y": y, "expert_id": cands, "gate": gate, "slot": slot, "drop": drop,
             "counts": counts, "aux_loss": aux_loss(r["probs"], counts),
             "logits": r["logits"], "probs": r["probs"], "capacity": C}
+
+
+# --------------------------------------------------------------------------
+# Backward of the top-1 layer, for the training step the pages describe
+# ([SWITCH] load-balancing section: the auxiliary loss is added to the
+# training loss with a coefficient alpha; [TOP1] load-balancing section:
+# L_aux = N * sum_i f_i P_i).  The loss seen here is <dy, y> + alpha * L_aux,
+# so dy is the upstream gradient of y.  Readings:
+#   * the routing decisions (argmax, capacity, slots) are piecewise constant
+#     and get no gradient; f_i (argmax counts) is constant, so
+#     dL_aux / dp[t, i] = N * f_i / T;
+#   * the gate gets dy_t . E(x_t) when gate_multiply is set (y_t = g_t E(x_t));
+#     a dropped token's expert branch is zero and passes no gradient;
+#   * ReLU's derivative at 0 is taken as 0.
+# Softmax backward: dl = p * (dp - sum_i p_i dp_i).
+# --------------------------------------------------------------------------
+def backward(x, W_g, W1, W2, capacity_factor: float, dy, priority_mode: int = TOKEN_ORDER,
+             gate_multiply: int = 1, b_g=None, W1s=None, W2s=None, aux_coef: float = 0.0):
+    """Gradients of <dy, y> + aux_coef * L_aux.  Returns a dict with dx,
+    dW_g, db_g, dW1, dW2 (and dW1s, dW2s with a shared expert), all fp64."""
+    fw = forward(x, W_g, W1, W2, capacity_factor, priority_mode, gate_multiply, b_g, W1s, W2s)
+    x64, dy64 = _f64(x), _f64(dy)
+    Wg64, W1_64, W2_64 = _f64(W_g), _f64(W1), _f64(W2)
+    T, d = x64.shape
+    N = Wg64.shape[0]
+    e, g, slot = fw["expert_id"], fw["gate"], fw["slot"]
+    dx = np.zeros_like(x64)
+    dW1 = np.zeros_like(W1_64)
+    dW2 = np.zeros_like(W2_64)
+    dgate = np.zeros(T)
+    for i in range(N):
+        rows = np.nonzero((e == i) & (slot >= 0))[0]
+        if rows.size == 0:
+            continue
+        xr = x64[rows]
+        hpre = xr @ W1_64[i].T                   # [n, F]
+        h = np.maximum(hpre, 0.0)
+        o = h @ W2_64[i].T                       # [n, d]: E(x)
+        scale = g[rows][:, None] if gate_multiply else 1.0
+        dO = scale * dy64[rows]                  # through y = g * E(x)
+        if gate_multiply:
+            dgate[rows] = np.sum(dy64[rows] * o, axis=1)
+        dW2[i] = dO.T @ h
+        dh = (dO @ W2_64[i]) * (hpre > 0)
+        dW1[i] = dh.T @ xr
+        dx[rows] += dh @ W1_64[i]
+    out = {"dW1": dW1, "dW2": dW2}
+    if W1s is not None:
+        W1s64, W2s64 = _f64(W1s), _f64(W2s)
+        hpre = x64 @ W1s64.T
+        h = np.maximum(hpre, 0.0)
+        out["dW2s"] = dy64.T @ h
+        dh = (dy64 @ W2s64) * (hpre > 0)
+        out["dW1s"] = dh.T @ x64
+        dx += dh @ W1s64
+    p = fw["probs"]
+    dp = np.zeros_like(p)
+    dp[np.arange(T), e] += dgate                 # the gate is p[t, e_t]
+    f = fw["counts"] / T
+    dp += aux_coef * N * f[None, :] / T          # dL_aux / dp[t, i]
+    dl = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+    out["dW_g"] = dl.T @ x64
+    out["db_g"] = dl.sum(axis=0)
+    dx += dl @ Wg64
+    out["dx"] = dx
+    out["forward"] = fw
+    return out
 
 
 def forward_rows(rows: Sequence[int], x, expert_id, gate, slot, gate_multiply: int,

@@ -777,3 +777,77 @@ def test_forward_rows_expert_choice_matches_forward():
     part = O.forward_rows_expert_choice(rows, x, full["chosen"], full["gates"], 1,
                                         lambda e: (W1[e], W2[e]), W1s, W2s)
     np.testing.assert_allclose(part, full["y"][rows], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------ backward
+def _loss(x, W_g, W1, W2, cf, dy, mode, gm, b_g, W1s, W2s, alpha):
+    f = O.forward(x, W_g, W1, W2, cf, mode, gm, b_g, W1s, W2s)
+    return float(np.sum(f["y"] * dy.numpy()) + alpha * f["aux_loss"]), f
+
+
+@pytest.mark.parametrize("mode,gm,shared,cf", [(0, 1, 0, 0.8), (1, 1, 1, 0.8), (0, 0, 0, 1.5),
+                                               (1, 0, 1, 0.6)])
+def test_backward_matches_central_differences(mode, gm, shared, cf):
+    """Every gradient of <dy, y> + alpha * L_aux against central differences
+    of the (pinned) forward, at entries whose perturbation leaves the
+    routing unchanged."""
+    rng = np.random.default_rng(31 + 2 * mode + gm)
+    T, d, F, N, alpha = 24, 6, 10, 3, 0.37
+    x = torch.tensor(rng.normal(size=(T, d)))
+    W_g = torch.tensor(rng.normal(size=(N, d)))
+    b_g = torch.tensor(rng.normal(size=N) * 0.3)
+    W1 = torch.tensor(rng.normal(size=(N, F, d)))
+    W2 = torch.tensor(rng.normal(size=(N, d, F)))
+    W1s = torch.tensor(rng.normal(size=(F, d))) if shared else None
+    W2s = torch.tensor(rng.normal(size=(d, F))) if shared else None
+    dy = torch.tensor(rng.normal(size=(T, d)))
+    g = O.backward(x, W_g, W1, W2, cf, dy, mode, gm, b_g, W1s, W2s, aux_coef=alpha)
+    fw = g["forward"]
+    assert 0 < fw["drop"].sum() < T or cf > 1
+    params = {"x": x, "W_g": W_g, "b_g": b_g, "W1": W1, "W2": W2}
+    grads = {"x": g["dx"], "W_g": g["dW_g"], "b_g": g["db_g"], "W1": g["dW1"], "W2": g["dW2"]}
+    if shared:
+        params.update(W1s=W1s, W2s=W2s)
+        grads.update(W1s=g["dW1s"], W2s=g["dW2s"])
+    eps, checked = 1e-6, 0
+    for name, tns in params.items():
+        flat = tns.view(-1)
+        for idx in rng.choice(flat.numel(), min(12, flat.numel()), replace=False):
+            old = float(flat[idx])
+            vals = []
+            for s in (1.0, -1.0):
+                flat[idx] = old + s * eps
+                a = dict(params)
+                lv, f2 = _loss(a["x"], a["W_g"], a["W1"], a["W2"], cf, dy, mode, gm, a["b_g"],
+                               a.get("W1s"), a.get("W2s"), alpha)
+                same = (np.array_equal(f2["expert_id"], fw["expert_id"])
+                        and np.array_equal(f2["slot"], fw["slot"]))
+                vals.append((lv, same))
+            flat[idx] = old
+            if not (vals[0][1] and vals[1][1]):
+                continue   # the routing moved: no derivative there
+            fd = (vals[0][0] - vals[1][0]) / (2 * eps)
+            an = float(np.asarray(grads[name]).reshape(-1)[idx])
+            assert abs(fd - an) <= 1e-5 * max(1.0, abs(an)), (name, int(idx), fd, an)
+            checked += 1
+    assert checked >= 40
+
+
+def test_backward_one_expert_is_the_dense_ffn_gradient():
+    """N = 1, nothing dropped: the gate is exactly 1 and the router gets no
+    gradient; the FFN gradients are those of a dense two-layer ReLU MLP,
+    from torch.autograd in float64."""
+    rng = np.random.default_rng(33)
+    T, d, F = 16, 5, 9
+    x = torch.tensor(rng.normal(size=(T, d)), requires_grad=True)
+    W1 = torch.tensor(rng.normal(size=(1, F, d)), requires_grad=True)
+    W2 = torch.tensor(rng.normal(size=(1, d, F)), requires_grad=True)
+    W_g = torch.tensor(rng.normal(size=(1, d)))
+    dy = torch.tensor(rng.normal(size=(T, d)))
+    y = torch.nn.functional.linear(torch.relu(torch.nn.functional.linear(x, W1[0])), W2[0])
+    (y * dy).sum().backward()
+    g = O.backward(x.detach(), W_g, W1.detach(), W2.detach(), 1.0, dy, aux_coef=0.5)
+    np.testing.assert_allclose(g["dx"], x.grad.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g["dW1"], W1.grad.numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(g["dW2"], W2.grad.numpy(), rtol=1e-12, atol=1e-12)
+    assert np.all(g["dW_g"] == 0) and np.all(g["db_g"] == 0)
