@@ -101,6 +101,42 @@ __device__ __forceinline__ void topk_candidates(At at, int N, int (&cand)[kMaxCa
     }
   }
 }
+// Adds one epilogue warp's 32-row x 32-token block of an expert output into
+// y with 16-byte atomic adds (several slots may add into one token's row).
+// On entry lane l holds rows r0 + l for tokens c0 .. c0 + 31 in v (column
+// jj in v[jj / 16][jj % 16]); token and gate of column c0 + l are in tk32 /
+// gv32.  The block is transposed by shuffles so that each lane adds 4
+// consecutive rows of one token: 8 vector adds per lane instead of 32
+// scalar ones.  ld: y's row stride; rows: rows of y (a multiple of 4).
+__device__ __forceinline__ void add_block_v4(float (&v)[2][16], int tk32, float gv32, float* y,
+                                             int ld, int r0, int rows, int c0, int nv,
+                                             int lane) {
+#pragma unroll
+  for (int jj = 0; jj < 32; ++jj) v[jj >> 4][jj & 15] *= __shfl_sync(0xffffffffu, gv32, jj);
+  const int rg = lane & 7;        // this lane's 4-row group
+  const int part = lane >> 3;     // which of 4 tokens per round it takes
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {   // round k: tokens 4k .. 4k + 3
+    float w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float got = 0.f;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float t = __shfl_sync(0xffffffffu, v[(4 * k + m) >> 4][(4 * k + m) & 15], rg * 4 + i);
+        if (part == m) got = t;
+      }
+      w[i] = got;
+    }
+    const int jj = 4 * k + part;
+    const int tj = __shfl_sync(0xffffffffu, tk32, jj);
+    const int r = r0 + 4 * rg;
+    if (c0 + jj < nv && r < rows)
+      atomicAdd(reinterpret_cast<float4*>(y + (size_t)tj * (size_t)ld + r),
+                make_float4(w[0], w[1], w[2], w[3]));
+  }
+}
+
 cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 // bf16 layers with N <= kMaxExpertsTc: W_g split into three bf16 pieces
 // [3][n_mma][d] (rows >= N zero), then the tensor-core router over them.

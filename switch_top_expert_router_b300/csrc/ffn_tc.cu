@@ -510,6 +510,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[2][16];
           fetch16(c0, v[0]);
           fetch16(c0 + 16, v[1]);
+          if constexpr (kAtomicY) {
+            add_block_v4(v, tk32, gv32, a.y, a.d, u.mt * kTileM + q * 32, a.d, c0, u.nv, lane);
+            continue;
+          }
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) {
             const int tj = __shfl_sync(kAll, tk32, jj);

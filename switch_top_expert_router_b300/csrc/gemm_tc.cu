@@ -381,6 +381,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[2][16];
           fetch16(c0, v[0]);
           fetch16(c0 + 16, v[1]);
+          if constexpr (kEpi == 3) {
+            add_block_v4(v, tk32, gv32, y, g.ldo, w.mt * kTileM + q * 32, g.M, c0, w.nv, lane);
+            continue;
+          }
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int tj = __shfl_sync(kAll, tk32, j);
