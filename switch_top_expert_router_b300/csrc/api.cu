@@ -109,6 +109,8 @@ struct Plan {
   int part_units;    // tail-split partial tiles of the tensor-core GEMMs
   // workspace offsets
   bool tc_router;    // bf16 x and N <= kMaxExpertsTc: tensor-core router
+  int rsplit;        // K splits of the tensor-core router (few tokens, long d_model)
+  size_t o_rpart;    // its partial logits [rsplit][T][N]
   size_t o_cand, o_candp, o_used;   // Expanded Drop and top-2
   size_t o_hist2, o_rank2, o_cnt2, o_e1, o_g1;   // top-2
   size_t o_probt, o_sgate;                        // expert choice; slot gates
@@ -221,6 +223,18 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
     q.o_g1 = take((size_t)q.T * 4);
   }
   q.tc_router = q.bf16 && q.N <= kMaxExpertsTc;
+  // Few tokens (at most 8 router tiles of 128) and a long d_model: one CTA
+  // per tile would walk every K block alone, so the K blocks are split over
+  // more CTAs (at least 4 blocks each); their sums are added and routed by
+  // the FFMA router's kernel.
+  q.rsplit = 1;
+  if (q.tc_router && q.N <= 128) {
+    const int64_t tiles = cdiv(q.T, 128), kbt = cdiv(q.d, kTileK);
+    if (tiles <= 8)
+      while (q.rsplit < 32 && tiles * q.rsplit * 2 <= kPlanSMs && kbt >= 8 * q.rsplit)
+        q.rsplit *= 2;
+  }
+  if (q.rsplit > 1) q.o_rpart = take((size_t)q.rsplit * q.T * q.N * 4);
   if (q.tc_router) q.o_wsplit = take((size_t)3 * router_tc_n_mma((int)q.N) * q.d * 2);
   if (need_gemm) {
     q.o_xbuf = take((size_t)NC * q.d * q.elem);
@@ -292,7 +306,22 @@ int launch_tc_router(const Plan& q, const RouterArgs& ra, void* ws, int* status,
   if (!make_map(&tx, ra.x, (uint64_t)q.T, (uint64_t)q.d, 128) ||
       !make_map(&tw, pieces, (uint64_t)3 * n_mma, (uint64_t)q.d, (uint32_t)n_mma))
     return SWITCH_MOE_ERR_CUDA;
-  if (launch_router_tc(ra, tx, tw, status, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+  if (q.rsplit == 1) {
+    if (launch_router_tc(ra, tx, tw, status, s, true) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
+    return SWITCH_MOE_OK;
+  }
+  // split along K: partial sums on the tensor cores, then the parts added in
+  // order (+ bias) and routed (or stored, for switch_moe_router_logits)
+  RouterArgs rp{};
+  rp.x = ra.x; rp.T = ra.T; rp.d = ra.d; rp.N = ra.N; rp.x_is_bf16 = 1;
+  rp.part_out = at<float>(ws, q.o_rpart);
+  if (launch_router_tc(rp, tx, tw, status, s, true, q.rsplit) != cudaSuccess)
+    return SWITCH_MOE_ERR_CUDA;
+  RouterArgs rr = ra;
+  rr.x = nullptr;
+  rr.parts_in = rp.part_out;
+  rr.n_parts = q.rsplit;
+  if (launch_router(rr, s) != cudaSuccess) return SWITCH_MOE_ERR_CUDA;
   return SWITCH_MOE_OK;
 }
 

@@ -67,6 +67,13 @@ struct RouterArgs {
   // expert choice: every probability, transposed (expert e's scores of all
   // tokens contiguous), or null
   float* probs_t;         // [N, T]
+  // Router split along K (few tokens, long d_model): the tensor-core router
+  // writes each K range's logit sums to part_out [split][T][N] (no bias, no
+  // routing); the FFMA router's kernel then routes sum_p parts_in[p] + b_g,
+  // parts in order.
+  float* part_out;
+  const float* parts_in;
+  int n_parts;
 };
 
 // A token's first kMaxCand experts by logit, descending, lowest index first
@@ -143,8 +150,9 @@ cudaError_t launch_router(const RouterArgs& a, cudaStream_t s);
 int router_tc_n_mma(int N);
 cudaError_t launch_split_wg(const float* W_g, __nv_bfloat16* pieces, int N, int d,
                             cudaStream_t s);
+// ksplit > 1 (N <= 128 only): K ranges over blockIdx.y, sums to a.part_out.
 cudaError_t launch_router_tc(const RouterArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                             int* status, cudaStream_t s, bool pdl = false);
+                             int* status, cudaStream_t s, bool pdl = false, int ksplit = 1);
 
 // ------------------------------------------------------- scan / tile lists
 struct ScanArgs {

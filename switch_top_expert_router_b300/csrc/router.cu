@@ -196,7 +196,18 @@ __global__ void __launch_bounds__(NTHREADS) router_kernel(RouterArgs a) {
   if (blockIdx.x == 0 && threadIdx.x == 0 && a.ctrl) {
     a.ctrl[0] = 0;   // done counter of the scan kernel that follows
   }
-  if (a.logits_in) {
+  if (a.parts_in) {   // K-split tensor-core logits: the parts in order, then the bias
+    for (int idx = threadIdx.x; idx < TM * a.N; idx += NTHREADS) {
+      const int r = idx / a.N, i = idx - r * a.N;
+      float v = 0.f;
+      if (t0 + r < a.T) {
+        for (int p = 0; p < a.n_parts; ++p) v += a.parts_in[((size_t)p * a.T + t0 + r) * a.N + i];
+        if (a.b_g) v += a.b_g[i];
+      }
+      lg[r * ldl + i] = v;
+    }
+    __syncthreads();
+  } else if (a.logits_in) {
     for (int idx = threadIdx.x; idx < TM * a.N; idx += NTHREADS) {
       int r = idx / a.N, i = idx - r * a.N;
       lg[r * ldl + i] = (t0 + r < a.T) ? a.logits_in[(size_t)(t0 + r) * a.N + i] : 0.f;

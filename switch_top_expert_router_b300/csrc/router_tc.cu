@@ -214,6 +214,15 @@ __device__ __forceinline__ void router_epilogue_regs(
     __syncwarp();
     if (lane == 0) mbar_arrive(&tempty[b]);
   }
+  if (a.part_out) {   // K split: this range's sums only; the FFMA kernel routes
+    if (valid) {
+      float* dst = a.part_out + ((size_t)blockIdx.y * a.T + t) * a.N;
+#pragma unroll
+      for (int i = 0; i < kRegExperts; ++i)
+        if (i < a.N) dst[i] = run[i];
+    }
+    return;
+  }
   // stage the finished logits (bias added) in the idle pipeline buffers
   float* lg = reinterpret_cast<float*>(tiles);
   float* row = lg + (size_t)(q * 32 + lane) * kEpiLd;
@@ -229,7 +238,8 @@ __device__ __forceinline__ void router_epilogue_regs(
 template <bool kRegs>
 __global__ void __launch_bounds__(kThreads, 1)
     router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                     const RouterArgs a, int n_mma, int k_blocks, int stages, int* status) {
+                     const RouterArgs a, int n_mma, int k_per, int k_total, int stages,
+                     int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t w_bytes = (uint32_t)n_mma * 128u;
@@ -249,6 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.N, T = a.T;
   const int t0 = blockIdx.x * 128;
+  // K range of this CTA (blockIdx.y > 0 only when the router is split along K)
+  const int kb0 = (int)blockIdx.y * k_per;
+  const int k_blocks = min(k_per, k_total - kb0);
   // TMEM: running sum at column 0, block accumulators after it
   const bool dbl = 3 * n_mma <= 512;
   const int nacc = dbl ? 2 : 1;
@@ -297,7 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int npre = min(stages, k_blocks);
       for (int kb = 0; kb < npre; ++kb) {
         mbar_arrive_expect_tx(&full[kb], stage_bytes);
-        tma_load_2d(tiles + (size_t)kb * stage_bytes, &tmX, &full[kb], kb * kTileK, t0, pol_x);
+        tma_load_2d(tiles + (size_t)kb * stage_bytes, &tmX, &full[kb], (kb0 + kb) * kTileK, t0,
+                    pol_x);
       }
       grid_dep_wait();
       grid_dep_launch();
@@ -305,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0;
       for (int kb = 0; kb < k_blocks; ++kb) {
         uint8_t* st = tiles + (size_t)stage * stage_bytes;
-        const int kx = kb * kTileK;
+        const int kx = (kb0 + kb) * kTileK;
         if (kb >= npre) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, status,
                          SWITCH_MOE_ERR_DEVICE_TIMEOUT))
@@ -579,7 +593,7 @@ cudaError_t launch_split_wg(const float* W_g, __nv_bfloat16* pieces, int N, int 
 }
 
 cudaError_t launch_router_tc(const RouterArgs& a, const CUtensorMap& tmX, const CUtensorMap& tmW,
-                             int* status, cudaStream_t s, bool pdl) {
+                             int* status, cudaStream_t s, bool pdl, int ksplit) {
   const int n_mma = router_tc_n_mma(a.N);
   const int stages = router_tc_stages(a.N, a.d);
   const size_t smem = router_tc_smem_bytes(a.N, a.d);
@@ -589,8 +603,10 @@ cudaError_t launch_router_tc(const RouterArgs& a, const CUtensorMap& tmX, const 
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
   const int grid = (a.T + 127) / 128;
-  return launch_k(kern, dim3(grid), dim3(kThreads), smem, s, pdl, tmX, tmW, a, n_mma,
-                  (a.d + kTileK - 1) / kTileK, stages, status);
+  const int k_total = (a.d + kTileK - 1) / kTileK;
+  const int k_per = (k_total + ksplit - 1) / ksplit;
+  return launch_k(kern, dim3(grid, ksplit), dim3(kThreads), smem, s, pdl, tmX, tmW, a, n_mma,
+                  k_per, k_total, stages, status);
 }
 
 }  // namespace smoe
