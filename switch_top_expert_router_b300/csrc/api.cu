@@ -189,7 +189,10 @@ int make_plan(const switch_moe_params* p, Plan* pl, bool need_gemm) {
   }
   q.max_entries = (int)(q.N * cdiv(C, q.BN));
   q.ksplit = 1;
-  if (q.bf16 && need_gemm) {
+  if (q.bf16 && need_gemm && q.BN > 128) {
+    // token tiles up to 128 run the one-launch FFN, which balances its own
+    // last wave (measured on the decode shape: 354 against 368 us with a
+    // K-split second GEMM and a separate combine)
     const int k2 = (int)cdiv(q.F, kTileK);
     q.ksplit = choose_ksplit((int64_t)q.max_entries * cdiv(q.d, kTileM), k2, kPlanSMs);
   }

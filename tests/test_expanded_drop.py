@@ -84,7 +84,8 @@ FWD_CASES = [
     ("bf16-shared-k3", 1000, 128, 256, 8, 0.8, "bf16", 3, 1, 0.6),
     ("f32-k2", 512, 64, 256, 8, 0.6, "f32", 2, 0, 1.5),
     ("bf16-big-C-k2", 3000, 128, 256, 4, 0.9, "bf16", 2, 0, 0.6),      # token tiles of 256
-    ("bf16-decode-ksplit-k2", 64, 512, 1024, 8, 0.9, "bf16", 2, 0, 0.6),  # K-split GEMM 2
+    ("bf16-decode-k2", 64, 512, 1024, 8, 0.9, "bf16", 2, 0, 0.6),   # 16-token tiles
+    ("bf16-ksplit-k2", 300, 512, 1024, 2, 1.0, "bf16", 2, 0, 1.5),  # C = 150: K-split GEMM 2
 ]
 
 

@@ -104,7 +104,8 @@ FWD_CASES = [
     ("f32", 512, 64, 256, 8, 1.0, "f32", 1, 0),
     ("f32-shared", 300, 64, 128, 4, 1.5, "f32", 1, 1),
     ("bf16-big-C", 3000, 128, 256, 4, 1.2, "bf16", 1, 0),          # token tiles of 256
-    ("bf16-decode-ksplit", 64, 512, 1024, 8, 1.0, "bf16", 1, 0),  # K-split GEMM 2
+    ("bf16-decode", 64, 512, 1024, 8, 1.0, "bf16", 1, 0),         # 16-token tiles
+    ("bf16-ksplit", 300, 512, 1024, 2, 1.0, "bf16", 1, 0),        # C = 150: K-split GEMM 2
     ("bf16-C-over-T", 40, 64, 128, 8, 16.0, "bf16", 1, 0),        # every expert takes all
 ]
 

@@ -40,7 +40,8 @@ SMALL = [
     ("bf16-no-gate-mul", 600, 128, 256, 8, 1.0, "bf16", 0, 0, 0),
     ("bf16-shared", 300, 128, 384, 4, 1.0, "bf16", 0, 1, 1),
     ("bf16-multi-token-tiles", 3000, 128, 256, 4, 1.0, "bf16", 0, 1, 0),  # C = 750: 3 tiles
-    ("bf16-decode-ksplit", 64, 512, 1024, 8, 2.0, "bf16", 0, 1, 0),       # K split of GEMM2
+    ("bf16-decode", 64, 512, 1024, 8, 2.0, "bf16", 0, 1, 0),       # 16-token tiles, one launch
+    ("bf16-ksplit", 300, 512, 1024, 2, 1.0, "bf16", 0, 1, 0),     # C = 150: K-split GEMM 2
     ("bf16-odd-d", 200, 72, 136, 3, 1.0, "bf16", 0, 1, 0),        # K and M tails (TMA zero fill)
     ("bf16-one-expert", 257, 128, 128, 1, 1.0, "bf16", 0, 1, 0),  # dense FFN
     ("bf16-one-token", 1, 64, 128, 4, 1.0, "bf16", 0, 1, 0),

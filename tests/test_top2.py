@@ -91,7 +91,8 @@ FWD_CASES = [
     ("f32", 512, 64, 256, 8, 1.0, "f32", 0, 0, 1.5),
     ("f32-shared", 300, 64, 128, 4, 1.5, "f32", 1, 1, 0.6),
     ("bf16-big-C", 3000, 128, 256, 4, 1.2, "bf16", 0, 0, 0.6),          # token tiles of 256
-    ("bf16-decode-ksplit", 64, 512, 1024, 8, 2.0, "bf16", 1, 0, 0.6),  # K-split GEMM 2
+    ("bf16-decode", 64, 512, 1024, 8, 2.0, "bf16", 1, 0, 0.6),      # 16-token tiles
+    ("bf16-ksplit", 300, 512, 1024, 2, 1.0, "bf16", 1, 0, 0.0),     # C = 150: K-split GEMM 2
     ("bf16-one-token", 1, 64, 128, 4, 1.0, "bf16", 1, 0, 0.0),
 ]
 
