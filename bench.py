@@ -49,8 +49,8 @@ from workloads import CONFIGS, expert_weights, make_inputs, zipf_bias  # noqa: E
 # it was taken on (sha256 of the .cu file); any other source reports null.
 NCU_TRAFFIC = {
     "base": {"source": "ffn_tc.cu",
-             "sha256": "a5146f7cec1dc865409a4d5070ad96fceda3457533920cbe7ff528ed7f46dd58",
-             "bytes_per_launch": (1266.141 + 85.651) * 1e6},
+             "sha256": "f5ef46009d9600e77aafa2ed11ec17daa742959dc9f87abfb7f69c01b4afded6",
+             "bytes_per_launch": (1266.399 + 87.187) * 1e6},
 }
 FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
