@@ -85,7 +85,8 @@ extern "C" int switch_moe_route_from_logits_noalloc(const switch_moe_params* p,
       (p->priority_mode != SWITCH_MOE_TOKEN_ORDER && p->priority_mode != SWITCH_MOE_GATE_PRIORITY))
     return SWITCH_MOE_ERR_INVALID_ARG;
   if (p->top_k < 0 || p->top_k > 2 || p->renormalize != 0) return SWITCH_MOE_ERR_INVALID_ARG;
-  if (p->expand > 1 || p->top_k > 1) return SWITCH_MOE_ERR_UNSUPPORTED;   // plain top-1 only
+  if (p->expand > 1 || p->top_k > 1 || p->expert_choice != 0)
+    return SWITCH_MOE_ERR_UNSUPPORTED;   // plain top-1 only
   // sizes past the static scratch are refused, never truncated
   if (p->T > kNoAllocMaxT || p->N > kNoAllocMaxN) return SWITCH_MOE_ERR_UNSUPPORTED;
   int* status = device_status_ptr();

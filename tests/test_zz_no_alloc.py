@@ -54,3 +54,13 @@ def test_noalloc_rejects_sizes_past_the_static_scratch(lib):
     logits = torch.zeros(64, 257, device="cuda")
     p = lib.make_params(64, 8, 8, 257, 1.0, 0, 1, lib.F32, 0)
     assert _raw_noalloc(lib, p, logits, _outs(64, 257)) == lib.SWITCH_MOE_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(expand=2), "UNSUPPORTED"), (dict(top_k=2), "UNSUPPORTED"),
+    (dict(expert_choice=1), "UNSUPPORTED"), (dict(renormalize=1), "INVALID_ARG"),
+])
+def test_noalloc_takes_plain_top1_only(lib, kw, code):
+    logits = torch.zeros(64, 8, device="cuda")
+    p = lib.make_params(64, 8, 8, 8, 1.0, 0, 1, lib.F32, 0, **kw)
+    assert _raw_noalloc(lib, p, logits, _outs(64, 8)) == getattr(lib, "SWITCH_MOE_ERR_" + code)
