@@ -9,7 +9,11 @@ One step = one switch_moe_forward() over one batch of the workload
 GEMM 2, combine).  Prints ONE JSON line (rank 0):
 
   value      tokens/s of the whole job, inputs resident in HBM, timed with
-             CUDA events over exactly K steps between barriers
+             CUDA events over exactly K steps between barriers; each step
+             replays the whole forward captured once into a CUDA graph (as
+             a serving loop does; eager calls are timed too, reported in
+             "timing", and are the fallback if capture fails; --eager
+             times eager calls only)
   e2e        the same through switch_moe_forward_hostio(): x copied from
              pinned host memory and every output copied back inside the
              timed region
@@ -70,11 +74,14 @@ def kernel_traffic(config: str):
 
 
 def gemm2_ksplit(w, C: int) -> int:
-    """K splits of the second routed GEMM, by the library's rule: split the
+    """K splits of the second routed GEMM, by the library's rule: token
+    tiles up to 128 take the one-launch FFN (no split); wider ones split the
     K = d_ff reduction (in powers of two, at most 8) only while there are
     fewer than two (expert, token tile, 128-row) tiles per SM of a 148-SM
     B300."""
     bn = min(-(-C // 16) * 16, 256)
+    if bn <= 128:
+        return 1
     tiles = w.N * -(-C // bn) * -(-w.d_model // 128)
     k_blocks = -(-w.d_ff // 64)
     s = 1
@@ -297,6 +304,8 @@ def main():
                     help="top-2 gates renormalised over the chosen pair")
     ap.add_argument("--expert-choice", type=int, default=0, choices=[0, 1],
                     help="expert-choice routing (each expert takes its C best tokens)")
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager calls only (no CUDA-graph replay)")
     ap.add_argument("--token-order", action="store_true",
                     help="token-order priority whatever the workload's (Expanded Drop "
                          "on the skewed shape)")
@@ -350,28 +359,54 @@ def main():
     if rc != 0:
         raise RuntimeError(f"device status after warm-up: {sm.strerror(rc)}")
 
+    # The whole forward captured once into a CUDA graph, as a serving loop
+    # replays it (same kernels, same work every step); eager calls are timed
+    # too, and are the fallback when capture is unavailable.
+    graph, graph_note = None, None
+    if not args.eager:
+        try:
+            cs = torch.cuda.Stream(dev)
+            g = torch.cuda.CUDAGraph()
+            torch.cuda.synchronize()
+            with torch.cuda.stream(cs):
+                with torch.cuda.graph(g, stream=cs):
+                    step()
+            torch.cuda.synchronize()
+            for _ in range(args.warmup):
+                g.replay()
+            torch.cuda.synchronize()
+            graph = g
+        except Exception as exc:   # noqa: BLE001 -- reported in the JSON line
+            graph_note = f"capture failed, eager timing: {exc!r}"[:200]
+
     # ---- timed region: exactly K steps
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    if pg:
-        pg.barrier()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    if pg:
-        pg.barrier()
-    ms = e0.elapsed_time(e1)
+
+    def timed(fn):
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        return e0.elapsed_time(e1)
+
+    ms = timed(graph.replay if graph else step)
+    eager_ms = timed(step) if graph else ms
     clk = clocks.stop()
     rc = sm.switch_moe_sync_status()
     if rc != 0:
         raise RuntimeError(f"device status after timing: {sm.strerror(rc)}")
     ms = max_over_ranks(ms, pg, dev)
+    eager_ms = max_over_ranks(eager_ms, pg, dev)
     value = job_tokens_per_s(w.T, args.steps, world, ms)
 
     # ---- per-phase times (same K steps, events at the phase boundaries)
@@ -430,7 +465,13 @@ def main():
     # ranking + dispatch], GEMM 1 [+ shared GEMMs], GEMM 2 [+ combine when the
     # second GEMM's epilogue cannot do it: fp32 layers, K-split GEMM 2]
     # [+ Expanded Drop passes and the moved rows' dispatch]
-    launches = ((2 if tc_router else 1) + 2 + (2 if w.priority_mode else 0)
+    # [+ the FFMA router kernel that adds the parts of a K-split
+    # tensor-core router: few tokens (<= 8 tiles of 128), long d_model]
+    tiles_r = -(-w.T // 128)
+    router_split = (tc_router and w.N <= 128 and tiles_r <= 8
+                    and -(-w.d_model // 64) >= 8 and tiles_r * 2 <= 148)
+    launches = ((2 if tc_router else 1) + (1 if router_split else 0) + 2
+                + (2 if w.priority_mode else 0)
                 + (1 if ffn_one else 2) + (2 if w.has_shared else 0) + (0 if fused else 1)
                 + (2 if args.expand > 1 else 0))
 
@@ -487,8 +528,12 @@ def main():
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": workload_config(w, args.expand, args.top_k, args.renormalize,
-                                      args.expert_choice),
+            "config": dict(workload_config(w, args.expand, args.top_k, args.renormalize,
+                                           args.expert_choice),
+                           launch=("CUDA-graph replay of the whole forward" if graph
+                                   else "eager calls")),
+            "timing": {"graph_replay": graph is not None, "eager_ms_per_step": eager_ms / args.steps,
+                       "note": graph_note},
             "e2e": e2e,
             "roofline": {"kernel": ("ffn_tc_kernel (expert GEMM 1 + 2, one launch)" if ffn_one
                                     else "gemm_tc_kernel (expert GEMM 1 + 2)"),
