@@ -252,6 +252,35 @@ int switch_moe_route_expert_choice(const switch_moe_params* p, const float* logi
                                    float* aux_loss, void* workspace, size_t workspace_bytes,
                                    switch_moe_stream_t stream);
 
+/* Backward of the top-1 layer ([SWITCH] load-balancing section: the
+ * auxiliary loss joins the training loss with a coefficient; [TOP1] core
+ * mechanism steps 1-3 and load-balancing section): the gradients of
+ * <dy, y> + aux_coef * L_aux with respect to x, W_g, b_g, W1, W2 (and W1s,
+ * W2s), where y is switch_moe_forward()'s output for the same inputs.
+ * Inputs: the forward's inputs (x, W_g, b_g, W1, W2, W1s, W2s; p as for the
+ *         forward), its routing outputs expert_id, gate, slot [T] and
+ *         expert_counts [N], and dy [T, d_model] fp32.
+ * Outputs (fp32, row-major, the layouts of the forward's operands):
+ *         dx [T, d_model]; dW_g [N, d_model]; db_g [N] (nullable: not
+ *         computed); dW1 [N, d_ff, d_model]; dW2 [N, d_model, d_ff]; dW1s
+ *         [d_ff, d_model], dW2s [d_model, d_ff] with a shared expert.
+ * Readings: the routing decisions (argmax, capacity, slots) are piecewise
+ * constant and get no gradient, so f_i is constant and dL_aux/dp[t, i] =
+ * N f_i / T; the gate gets dy . E(x) when gate_multiply is set; ReLU'(0) = 0.
+ * The forward's intermediates are recomputed in fp32 from the inputs (bf16
+ * inputs widened exactly) on FFMA.  Top-1 only (expand, top_k and
+ * expert_choice give SWITCH_MOE_ERR_UNSUPPORTED).  Workspace: at least
+ * switch_moe_backward_workspace_bytes(p); alignment and errors as for
+ * switch_moe_forward(). */
+int switch_moe_backward_workspace_bytes(const switch_moe_params* p, size_t* bytes);
+int switch_moe_backward(const switch_moe_params* p, const void* x, const float* W_g,
+                        const float* b_g, const void* W1, const void* W2, const void* W1s,
+                        const void* W2s, const int32_t* expert_id, const float* gate,
+                        const int32_t* slot, const int32_t* expert_counts, const float* dy,
+                        float aux_coef, float* dx, float* dW_g, float* db_g, float* dW1,
+                        float* dW2, float* dW1s, float* dW2s, void* workspace,
+                        size_t workspace_bytes, switch_moe_stream_t stream);
+
 /* Step 1 alone: logits [T, N] fp32 = x W_g^T (+ b_g), computed by the same
  * device code that switch_moe_forward() fuses with steps 2-4, so feeding
  * these logits to switch_moe_route_from_logits() reproduces the forward

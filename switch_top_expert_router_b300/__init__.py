@@ -51,7 +51,8 @@ EXPORTED = (
     "switch_moe_sync_status", "switch_moe_strerror", "switch_moe_version",
     "switch_moe_selftest_wait_timeout", "switch_moe_set_phase_events",
     "switch_moe_route_from_logits_noalloc", "switch_moe_forward_expert_choice",
-    "switch_moe_route_expert_choice",
+    "switch_moe_route_expert_choice", "switch_moe_backward_workspace_bytes",
+    "switch_moe_backward",
 )
 NUM_PHASE_EVENTS = 8
 PHASES = ("router", "scan_aux", "slots_dispatch", "shared_gemms", "expert_gemm1",
@@ -97,6 +98,12 @@ def _load() -> ctypes.CDLL:
     lib.switch_moe_forward_expert_choice.restype = I32
     lib.switch_moe_route_expert_choice.argtypes = [P, V, V, V, V, V, V, V, ctypes.c_size_t, V]
     lib.switch_moe_route_expert_choice.restype = I32
+    lib.switch_moe_backward_workspace_bytes.argtypes = [P, SZ]
+    lib.switch_moe_backward_workspace_bytes.restype = I32
+    # p, 7 inputs, 4 routing outputs, dy, aux_coef, 7 gradients, workspace, size, stream
+    lib.switch_moe_backward.argtypes = ([P] + [V] * 12 + [ctypes.c_float] + [V] * 8
+                                        + [ctypes.c_size_t, V])
+    lib.switch_moe_backward.restype = I32
     lib.switch_moe_forward_hostio.argtypes = fwd
     lib.switch_moe_forward_hostio.restype = I32
     lib.switch_moe_route_from_logits.argtypes = [P, V, V, V, V, V, V, V, V, ctypes.c_size_t, V]
@@ -484,6 +491,63 @@ def switch_moe_route_expert_choice(logits: torch.Tensor, capacity_factor: float,
             ctypes.c_size_t(ws.numel()), _stream(stream))
     _check(rc, "switch_moe_route_expert_choice")
     return o
+
+
+class BackwardOut(NamedTuple):
+    dx: torch.Tensor                 # [T, d_model] fp32
+    dW_g: torch.Tensor               # [N, d_model]
+    db_g: Optional[torch.Tensor]     # [N] (None without b_g)
+    dW1: torch.Tensor                # [N, d_ff, d_model]
+    dW2: torch.Tensor                # [N, d_model, d_ff]
+    dW1s: Optional[torch.Tensor]     # [d_ff, d_model] with a shared expert
+    dW2s: Optional[torch.Tensor]     # [d_model, d_ff]
+
+
+def switch_moe_backward_workspace_bytes(p: Params) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.switch_moe_backward_workspace_bytes(ctypes.byref(p), ctypes.byref(n)),
+           "switch_moe_backward_workspace_bytes")
+    return int(n.value)
+
+
+def switch_moe_backward(x: torch.Tensor, W_g: torch.Tensor, W1: torch.Tensor, W2: torch.Tensor,
+                        capacity_factor: float, fwd: ForwardOut, dy: torch.Tensor,
+                        aux_coef: float = 0.0, priority_mode: int = TOKEN_ORDER,
+                        gate_multiply: int = 1, b_g: Optional[torch.Tensor] = None,
+                        W1s: Optional[torch.Tensor] = None, W2s: Optional[torch.Tensor] = None,
+                        ws: Optional[torch.Tensor] = None, stream=None) -> BackwardOut:
+    """Gradients of <dy, y> + aux_coef * L_aux for the forward that produced
+    ``fwd`` (its routing outputs are reused); see switch_moe_backward in
+    include/switch_moe.h."""
+    dev = x.device
+    _contig(x, "x", None, dev)
+    _contig(dy, "dy", torch.float32, dev)
+    T, d, F, N = _layer_args(x, W_g, W1, W2, b_g, W1s, W2s, dev)
+    if dy.shape != (T, d):
+        raise ValueError("dy must be [T, d_model]")
+    for name, t, n in (("expert_id", fwd.expert_id, T), ("gate", fwd.gate, T),
+                       ("slot", fwd.slot, T), ("expert_counts", fwd.expert_counts, N)):
+        if t.numel() != n or not t.is_contiguous() or t.device != dev:
+            raise ValueError(f"fwd.{name} must be a contiguous {n}-element tensor on {dev}")
+    p = make_params(T, d, F, N, capacity_factor, priority_mode, gate_multiply, _dtype_code(x),
+                    int(W1s is not None))
+    if ws is None:
+        ws = workspace(switch_moe_backward_workspace_bytes(p), dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = BackwardOut(torch.empty((T, d), **f32), torch.empty((N, d), **f32),
+                      torch.empty(N, **f32) if b_g is not None else None,
+                      torch.empty((N, F, d), **f32), torch.empty((N, d, F), **f32),
+                      torch.empty((F, d), **f32) if W1s is not None else None,
+                      torch.empty((d, F), **f32) if W1s is not None else None)
+    with torch.cuda.device(dev):
+        rc = _lib.switch_moe_backward(
+            ctypes.byref(p), _ptr(x), _ptr(W_g), _ptr(b_g), _ptr(W1), _ptr(W2), _ptr(W1s),
+            _ptr(W2s), _ptr(fwd.expert_id), _ptr(fwd.gate), _ptr(fwd.slot),
+            _ptr(fwd.expert_counts), _ptr(dy), ctypes.c_float(aux_coef), _ptr(out.dx),
+            _ptr(out.dW_g), _ptr(out.db_g), _ptr(out.dW1), _ptr(out.dW2), _ptr(out.dW1s),
+            _ptr(out.dW2s), _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check(rc, "switch_moe_backward")
+    return out
 
 
 def switch_moe_router_logits(x: torch.Tensor, W_g: torch.Tensor,

@@ -916,6 +916,179 @@ int switch_moe_route_expert_choice(const switch_moe_params* p, const float* logi
   return rc;
 }
 
+// ------------------------------------------------------------ backward
+namespace {
+
+struct BwdPlan {
+  size_t o_Xg, o_dO, o_O, o_dX, o_H, o_dH, o_L, o_dgate, o_tok, o_Hs, o_dHs, total;
+};
+
+int make_bwd_plan(const switch_moe_params* p, Plan* q, BwdPlan* b) {
+  int rc = make_plan(p, q, true);
+  if (rc) return rc;
+  if (q->expand > 1 || q->topk > 1 || q->ec) return SWITCH_MOE_ERR_UNSUPPORTED;   // top-1 only
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+  const size_t NC = (size_t)q->N * (q->T ? q->C : 0);
+  b->o_Xg = take(NC * q->d * 4);
+  b->o_dO = take(NC * q->d * 4);
+  b->o_O = take(NC * q->d * 4);
+  b->o_dX = take(NC * q->d * 4);
+  b->o_H = take(NC * q->F * 4);
+  b->o_dH = take(NC * q->F * 4);
+  b->o_L = take((size_t)q->T * q->N * 4);
+  b->o_dgate = take((size_t)q->T * 4);
+  b->o_tok = take(NC * 4);
+  b->o_Hs = q->shared ? take((size_t)q->T * q->F * 4) : 0;
+  b->o_dHs = q->shared ? take((size_t)q->T * q->F * 4) : 0;
+  b->total = o;
+  return SWITCH_MOE_OK;
+}
+
+BGemmArgs bg(int M, int N, int K, int batches, float* C, bool acc = false) {
+  BGemmArgs g{};
+  g.M = M; g.N = N; g.K = K; g.batches = batches; g.C = C; g.accumulate = acc;
+  return g;
+}
+
+}  // namespace
+
+int switch_moe_backward_workspace_bytes(const switch_moe_params* p, size_t* bytes) {
+  if (!bytes) return SWITCH_MOE_ERR_INVALID_ARG;
+  Plan q;
+  BwdPlan b;
+  const int rc = make_bwd_plan(p, &q, &b);
+  if (rc) return rc;
+  *bytes = b.total;
+  return SWITCH_MOE_OK;
+}
+
+int switch_moe_backward(const switch_moe_params* p, const void* x, const float* W_g,
+                        const float* b_g, const void* W1, const void* W2, const void* W1s,
+                        const void* W2s, const int32_t* expert_id, const float* gate,
+                        const int32_t* slot, const int32_t* expert_counts, const float* dy,
+                        float aux_coef, float* dx, float* dW_g, float* db_g, float* dW1,
+                        float* dW2, float* dW1s, float* dW2s, void* workspace,
+                        size_t workspace_bytes, switch_moe_stream_t stream) {
+  Plan q;
+  BwdPlan bp;
+  int rc = make_bwd_plan(p, &q, &bp);
+  if (rc) return rc;
+  if (!std::isfinite(aux_coef)) return SWITCH_MOE_ERR_INVALID_ARG;
+  const DeviceInfo* dev = current_device();
+  if (!dev) return SWITCH_MOE_ERR_NO_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int T = (int)q.T, N = (int)q.N, d = (int)q.d, F = (int)q.F, C = q.C;
+  if (!dW_g || !dW1 || !dW2 || (q.shared && (!dW1s || !dW2s))) return SWITCH_MOE_ERR_INVALID_ARG;
+  if (T == 0) {   // no tokens: every gradient is zero
+    if (cudaMemsetAsync(dW_g, 0, (size_t)N * d * 4, s) != cudaSuccess ||
+        (db_g && cudaMemsetAsync(db_g, 0, (size_t)N * 4, s) != cudaSuccess) ||
+        cudaMemsetAsync(dW1, 0, (size_t)N * F * d * 4, s) != cudaSuccess ||
+        cudaMemsetAsync(dW2, 0, (size_t)N * d * F * 4, s) != cudaSuccess ||
+        (q.shared && (cudaMemsetAsync(dW1s, 0, (size_t)F * d * 4, s) != cudaSuccess ||
+                      cudaMemsetAsync(dW2s, 0, (size_t)d * F * 4, s) != cudaSuccess)))
+      return SWITCH_MOE_ERR_CUDA;
+    return SWITCH_MOE_OK;
+  }
+  if (!x || !W_g || !W1 || !W2 || !expert_id || !gate || !slot || !expert_counts || !dy || !dx ||
+      !workspace || (q.shared && (!W1s || !W2s)))
+    return SWITCH_MOE_ERR_INVALID_ARG;
+  if (!al(x, 16) || !al(W_g, 16) || !al(W1, 16) || !al(W2, 16) || !al(dy, 16) || !al(dx, 16) ||
+      !al(workspace, 256) || !al(expert_id, 4) || !al(gate, 4) || !al(slot, 4) ||
+      !al(expert_counts, 4) || !al(dW_g, 4) || !al(dW1, 4) || !al(dW2, 4) ||
+      (b_g && !al(b_g, 4)) || (db_g && !al(db_g, 4)) ||
+      (q.shared && (!al(W1s, 16) || !al(W2s, 16) || !al(dW1s, 4) || !al(dW2s, 4))))
+    return SWITCH_MOE_ERR_ALIGNMENT;
+  if (workspace_bytes < bp.total) return SWITCH_MOE_ERR_WORKSPACE_TOO_SMALL;
+  const bool bf = q.bf16;
+  void* ws = workspace;
+  BwdArgs a{};
+  a.T = T; a.N = N; a.C = C; a.d = d; a.gate_multiply = q.gm; a.aux_coef = aux_coef;
+  a.expert_id = expert_id; a.slot = slot; a.counts = expert_counts; a.gate = gate; a.dy = dy;
+  a.Xg = at<float>(ws, bp.o_Xg); a.dO = at<float>(ws, bp.o_dO); a.O = at<float>(ws, bp.o_O);
+  a.dX = at<float>(ws, bp.o_dX); a.dx = dx; a.dgate = at<float>(ws, bp.o_dgate);
+  a.L = at<float>(ws, bp.o_L); a.b_g = b_g; a.tok = at<int32_t>(ws, bp.o_tok);
+  float* H = at<float>(ws, bp.o_H);
+  float* dH = at<float>(ws, bp.o_dH);
+  const size_t Cd = (size_t)C * d, CF = (size_t)C * F, Fd = (size_t)F * d;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ok(cudaMemsetAsync(dx, 0, (size_t)T * d * 4, s)) || !ok(launch_bwd_gather(a, x, bf, s)))
+    return SWITCH_MOE_ERR_CUDA;
+  // routed experts, per expert e over its kept slots (min(count_e, C) rows)
+  BGemmArgs g = bg(C, F, d, N, H);                       // Hpre = Xg W1^T
+  g.mcount = expert_counts;
+  g.a_b = Cd; g.a_m = d; g.a_k = 1; g.b_b = Fd; g.b_n = d; g.b_k = 1;
+  g.c_b = CF; g.c_m = F; g.c_n = 1;
+  if (!ok(launch_bgemm(g, a.Xg, false, W1, bf, s)) ||
+      !ok(launch_bwd_relu(H, expert_counts, C, F, N, s)))   // H = relu(Hpre)
+    return SWITCH_MOE_ERR_CUDA;
+  if (q.gm) {
+    g = bg(C, d, F, N, a.O);                              // O = H W2^T
+    g.mcount = expert_counts;
+    g.a_b = CF; g.a_m = F; g.a_k = 1; g.b_b = Fd; g.b_n = F; g.b_k = 1;
+    g.c_b = Cd; g.c_m = d; g.c_n = 1;
+    if (!ok(launch_bgemm(g, H, false, W2, bf, s))) return SWITCH_MOE_ERR_CUDA;
+  }
+  g = bg(C, F, d, N, dH);                                 // dH = dO W2
+  g.mcount = expert_counts;
+  g.a_b = Cd; g.a_m = d; g.a_k = 1; g.b_b = Fd; g.b_n = 1; g.b_k = F;
+  g.c_b = CF; g.c_m = F; g.c_n = 1;
+  if (!ok(launch_bgemm(g, a.dO, false, W2, bf, s)) ||
+      !ok(launch_bwd_mask(dH, H, expert_counts, C, F, N, s)))   // through the ReLU
+    return SWITCH_MOE_ERR_CUDA;
+  g = bg(C, d, F, N, a.dX);                               // dX = dH W1
+  g.mcount = expert_counts;
+  g.a_b = CF; g.a_m = F; g.a_k = 1; g.b_b = Fd; g.b_n = 1; g.b_k = d;
+  g.c_b = Cd; g.c_m = d; g.c_n = 1;
+  if (!ok(launch_bgemm(g, dH, false, W1, bf, s))) return SWITCH_MOE_ERR_CUDA;
+  g = bg(d, F, C, N, dW2);                                // dW2 = dO^T H over the slots
+  g.kcount = expert_counts;
+  g.a_b = Cd; g.a_m = 1; g.a_k = d; g.b_b = CF; g.b_n = 1; g.b_k = F;
+  g.c_b = Fd; g.c_m = F; g.c_n = 1;
+  if (!ok(launch_bgemm(g, a.dO, false, H, false, s))) return SWITCH_MOE_ERR_CUDA;
+  g = bg(F, d, C, N, dW1);                                // dW1 = dH^T Xg over the slots
+  g.kcount = expert_counts;
+  g.a_b = CF; g.a_m = 1; g.a_k = F; g.b_b = Cd; g.b_n = 1; g.b_k = d;
+  g.c_b = Fd; g.c_m = d; g.c_n = 1;
+  if (!ok(launch_bgemm(g, dH, false, a.Xg, false, s)) || !ok(launch_bwd_scatter(a, s)))
+    return SWITCH_MOE_ERR_CUDA;
+  if (q.shared) {   // the shared expert, on every token with gate 1
+    float* Hs = at<float>(ws, bp.o_Hs);
+    float* dHs = at<float>(ws, bp.o_dHs);
+    g = bg(T, F, d, 1, Hs);
+    g.a_m = d; g.a_k = 1; g.b_n = d; g.b_k = 1; g.c_m = F; g.c_n = 1;
+    if (!ok(launch_bgemm(g, x, bf, W1s, bf, s)) || !ok(launch_bwd_relu(Hs, nullptr, T, F, 1, s)))
+      return SWITCH_MOE_ERR_CUDA;
+    g = bg(T, F, d, 1, dHs);
+    g.a_m = d; g.a_k = 1; g.b_n = 1; g.b_k = F; g.c_m = F; g.c_n = 1;
+    if (!ok(launch_bgemm(g, dy, false, W2s, bf, s)) ||
+        !ok(launch_bwd_mask(dHs, Hs, nullptr, T, F, 1, s)))
+      return SWITCH_MOE_ERR_CUDA;
+    g = bg(d, F, T, 1, dW2s);
+    g.a_m = 1; g.a_k = d; g.b_n = 1; g.b_k = F; g.c_m = F; g.c_n = 1;
+    if (!ok(launch_bgemm(g, dy, false, Hs, false, s))) return SWITCH_MOE_ERR_CUDA;
+    g = bg(F, d, T, 1, dW1s);
+    g.a_m = 1; g.a_k = F; g.b_n = 1; g.b_k = d; g.c_m = d; g.c_n = 1;
+    if (!ok(launch_bgemm(g, dHs, false, x, bf, s))) return SWITCH_MOE_ERR_CUDA;
+    g = bg(T, d, F, 1, dx, true);
+    g.a_m = F; g.a_k = 1; g.b_n = 1; g.b_k = d; g.c_m = d; g.c_n = 1;
+    if (!ok(launch_bgemm(g, dHs, false, W1s, bf, s))) return SWITCH_MOE_ERR_CUDA;
+  }
+  // router: logits again, then the softmax backward through the gate and L_aux
+  g = bg(T, N, d, 1, a.L);
+  g.a_m = d; g.a_k = 1; g.b_n = d; g.b_k = 1; g.c_m = N; g.c_n = 1;
+  if (!ok(launch_bgemm(g, x, bf, W_g, false, s)) || !ok(launch_bwd_router(a, s)))
+    return SWITCH_MOE_ERR_CUDA;
+  if (db_g && !ok(launch_bwd_colsum(a.L, db_g, T, N, s))) return SWITCH_MOE_ERR_CUDA;
+  g = bg(N, d, T, 1, dW_g);                               // dW_g = dl^T x over the tokens
+  g.a_m = 1; g.a_k = N; g.b_n = 1; g.b_k = d; g.c_m = d; g.c_n = 1;
+  if (!ok(launch_bgemm(g, a.L, false, x, bf, s))) return SWITCH_MOE_ERR_CUDA;
+  g = bg(T, d, N, 1, dx, true);                           // dx += dl W_g
+  g.a_m = N; g.a_k = 1; g.b_n = 1; g.b_k = d; g.c_m = d; g.c_n = 1;
+  if (!ok(launch_bgemm(g, a.L, false, W_g, false, s))) return SWITCH_MOE_ERR_CUDA;
+  return SWITCH_MOE_OK;
+}
+
 int switch_moe_router_logits(const switch_moe_params* p, const void* x, const float* W_g,
                              const float* b_g, float* logits, void* workspace,
                              size_t workspace_bytes, switch_moe_stream_t stream) {

@@ -403,6 +403,52 @@ struct SlotCombineArgs {
 };
 cudaError_t launch_combine_slots(const SlotCombineArgs& a, cudaStream_t s, bool pdl = false);
 
+// ------------------------------------------------------- backward
+// Strided batched fp32 GEMM: C_b[m, n] (+)= sum_k A_b[m, k] B_b[n, k], with
+// A_b[m, k] = A[b a_b + m a_m + k a_k] (B and C likewise); per-batch counts
+// (null: the full M, N, K) limit batch b's rows and reduction.
+struct BGemmArgs {
+  int M, N, K, batches;
+  const int32_t* mcount;
+  const int32_t* ncount;
+  const int32_t* kcount;
+  size_t a_b, a_m, a_k;
+  size_t b_b, b_n, b_k;
+  size_t c_b, c_m, c_n;
+  float* C;
+  int accumulate;
+};
+cudaError_t launch_bgemm(const BGemmArgs& g, const void* A, bool a_bf16, const void* B,
+                         bool b_bf16, cudaStream_t s);
+
+struct BwdArgs {
+  int T, N, C, d;
+  int gate_multiply;
+  float aux_coef;
+  const int32_t* expert_id;   // [T] forward's top-1 expert
+  const int32_t* slot;        // [T] forward's slot, -1 dropped
+  const int32_t* counts;      // [N] forward's expert_counts (f_i)
+  const float* gate;          // [T]
+  const float* dy;            // [T, d] upstream gradient of y
+  float* Xg;                  // [N C, d] dispatched rows (fp32)
+  float* dO;                  // [N C, d] gradient of each slot's expert output
+  float* O;                   // [N C, d] each slot's expert output E(x)
+  float* dX;                  // [N C, d] gradient of each slot's input row
+  float* dx;                  // [T, d] out
+  float* dgate;               // [T] gradient of the gate
+  float* L;                   // [T, N] logits without the bias in, router logit gradient out
+  const float* b_g;           // [N] or null
+  int32_t* tok;               // [N C] token of each slot
+};
+cudaError_t launch_bwd_gather(const BwdArgs& a, const void* x, bool x_bf16, cudaStream_t s);
+cudaError_t launch_bwd_relu(float* H, const int32_t* counts, int C, int F, int N,
+                            cudaStream_t s);
+cudaError_t launch_bwd_mask(float* dH, const float* H, const int32_t* counts, int C, int F,
+                            int batches, cudaStream_t s);
+cudaError_t launch_bwd_scatter(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_router(const BwdArgs& a, cudaStream_t s);
+cudaError_t launch_bwd_colsum(const float* dl, float* out, int T, int N, cudaStream_t s);
+
 // status word of the current device (see switch_moe_sync_status)
 int* device_status_ptr();
 
