@@ -286,6 +286,87 @@ def workload_config(w, expand=1, top_k=1, renormalize=0, expert_choice=0):
                   "(far above the 126 MB L2) from HBM"}
 
 
+FP32_FFMA_TFLOPS = 148 * 128 * 2 * 2.032 / 1e3   # B300: SMs x FP32 lanes x 2 flop x max GHz
+
+
+def run_backward(args, sm, rank, world, local):
+    """--backward: K calls of switch_moe_backward on the workload (the
+    forward's routing computed once before), timed with CUDA events.  The
+    backward runs on FFMA, so its roofline is the fp32 FMA peak (148 SMs x
+    128 lanes x 2 flop at the 2032 MHz maximum clock); its algorithmic
+    flops are 12 kept x d x F (six slot-sized contractions: the hidden
+    activation, the expert output, dH, dX, dW1, dW2) + 6 T N d (router
+    logits, dW_g, dx through W_g), shared expert extra."""
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    w = CONFIGS[args.config]
+    if args.token_order:
+        w = w.replace(priority_mode=0)
+    inp = make_inputs(w, seed=0, device=dev)
+    dy = torch.randn(w.T, w.d_model, generator=torch.Generator().manual_seed(7)).to(dev)
+    alpha = 0.01
+    fwd = sm.switch_moe_forward(inp.x, inp.W_g, inp.W1, inp.W2, w.capacity_factor,
+                                w.priority_mode, w.gate_multiply, b_g=inp.b_g, W1s=inp.W1s,
+                                W2s=inp.W2s)
+    p = sm.make_params(w.T, w.d_model, w.d_ff, w.N, w.capacity_factor, w.priority_mode,
+                       w.gate_multiply, sm.BF16 if w.dtype == "bf16" else sm.F32, w.has_shared)
+    ws = sm.workspace(sm.switch_moe_backward_workspace_bytes(p), dev)
+
+    def step():
+        sm.switch_moe_backward(inp.x, inp.W_g, inp.W1, inp.W2, w.capacity_factor, fwd, dy,
+                               aux_coef=alpha, priority_mode=w.priority_mode,
+                               gate_multiply=w.gate_multiply, b_g=inp.b_g, W1s=inp.W1s,
+                               W2s=inp.W2s, ws=ws)
+
+    for _ in range(args.warmup):
+        step()
+    stream = torch.cuda.current_stream(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), pg, dev)
+    clk = clocks.stop()
+    rc = sm.switch_moe_sync_status()
+    if rc != 0:
+        raise RuntimeError(f"device status after timing: {sm.strerror(rc)}")
+    C = sm.switch_moe_capacity(w.T, w.N, w.capacity_factor)
+    kept = int(torch.clamp(fwd.expert_counts, max=C).sum())
+    d, F = w.d_model, w.d_ff
+    flops = (2.0 * kept * d * F * (6 if w.gate_multiply else 5) + 6.0 * w.T * w.N * w.d_model
+             + (10.0 * w.T * d * F if w.has_shared else 0.0))
+    achieved = flops / (ms / args.steps / 1e3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": "top-1 MoE layer backward tokens/sec",
+            "value": w.T * args.steps * world / (ms / 1e3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_config(w), pass_="backward"),
+            "roofline": {"kernel": "bgemm_kernel (fp32 FFMA, every contraction of the backward)",
+                         "bound": "alu", "achieved": achieved, "peak": FP32_FFMA_TFLOPS,
+                         "unit": "TFLOP/s", "frac": achieved / FP32_FFMA_TFLOPS,
+                         "peak_kind": "derived: 148 SMs x 128 FP32 lanes x 2 flop x 2032 MHz",
+                         "traffic": None, "algorithmic_flops_per_step": flops},
+            "cpu_baseline": None, "e2e": None,
+            "gpu_launches": None, "clocks": clk}), flush=True)
+
+
 # ------------------------------------------------------------------ GPU arm
 def main():
     ap = argparse.ArgumentParser()
@@ -304,6 +385,8 @@ def main():
                     help="top-2 gates renormalised over the chosen pair")
     ap.add_argument("--expert-choice", type=int, default=0, choices=[0, 1],
                     help="expert-choice routing (each expert takes its C best tokens)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time switch_moe_backward (gradients of <dy, y> + alpha L_aux) instead")
     ap.add_argument("--eager", action="store_true",
                     help="time eager calls only (no CUDA-graph replay)")
     ap.add_argument("--token-order", action="store_true",
@@ -321,6 +404,8 @@ def main():
     import switch_top_expert_router_b300 as sm
     sm.load_library()
     torch.cuda.set_device(local)
+    if args.backward:
+        return run_backward(args, sm, rank, world, local)
     dev = torch.device("cuda", local)
     pg = None
     if world > 1:

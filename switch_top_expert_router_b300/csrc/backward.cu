@@ -27,8 +27,8 @@
 namespace smoe {
 namespace {
 
-constexpr int kTM = 64, kTN = 64, kTK = 16;   // output tile, K step
-constexpr int kBThreads = 256;                // 16 x 16 threads, 4 x 4 outputs each
+constexpr int kTM = 128, kTN = 128, kTK = 8;   // output tile, K step
+constexpr int kBThreads = 256;                  // 16 x 16 threads, 8 x 8 outputs each
 
 __device__ __forceinline__ float ld_as_float(const float* p, size_t i) { return p[i]; }
 __device__ __forceinline__ float ld_as_float(const __nv_bfloat16* p, size_t i) {
@@ -38,12 +38,14 @@ __device__ __forceinline__ float ld_as_float(const __nv_bfloat16* p, size_t i) {
 // C_b[m, n] (+)= sum_k A_b[m, k] * B_b[n, k] for batch b = blockIdx.z, with
 // A_b[m, k] = A[b * a_b + m * a_m + k * a_k] (B likewise) and
 // C_b[m, n] = C[b * c_b + m * c_m + n * c_n].  Per-batch counts (null: the
-// full M, N, K) limit the rows m, n and the reduction k of batch b.
+// full M, N, K) limit the rows m, n and the reduction k of batch b.  Each
+// thread holds an 8 x 8 block of the 128 x 128 tile; the K step of 8 is
+// staged in shared memory, loaded along each operand's contiguous axis.
 template <typename TA, typename TB>
-__global__ void __launch_bounds__(kBThreads) bgemm_kernel(BGemmArgs g, const TA* __restrict__ A,
+__global__ void __launch_bounds__(kBThreads, 2) bgemm_kernel(BGemmArgs g, const TA* __restrict__ A,
                                                           const TB* __restrict__ B) {
-  __shared__ float as[kTK][kTM + 4];
-  __shared__ float bs[kTK][kTN + 4];
+  __shared__ __align__(16) float as[kTK][kTM + 4];
+  __shared__ __align__(16) float bs[kTK][kTN + 4];
   const int b = blockIdx.z;
   const int M = g.mcount ? min(__ldg(g.mcount + b), g.M) : g.M;
   const int N = g.ncount ? min(__ldg(g.ncount + b), g.N) : g.N;
@@ -52,49 +54,76 @@ __global__ void __launch_bounds__(kBThreads) bgemm_kernel(BGemmArgs g, const TA*
   if (m0 >= M || n0 >= N) return;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
   const size_t ab = (size_t)b * g.a_b, bb = (size_t)b * g.b_b;
-  // load mapping: consecutive threads walk the operand's contiguous axis
   const bool a_k_fast = g.a_k == 1, b_k_fast = g.b_k == 1;
-  float acc[4][4];
+  float acc[8][8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < 8; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  for (int k0 = 0; k0 < K; k0 += kTK) {
-    for (int i = tid; i < kTM * kTK; i += kBThreads) {
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  // the next K step's operands are loaded into registers while this one's
+  // FMAs run (one shared-memory stage, one register stage)
+  constexpr int kRA = kTM * kTK / kBThreads, kRB = kTN * kTK / kBThreads;
+  float ra[kRA], rb[kRB];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int r = 0; r < kRA; ++r) {
+      const int i = tid + r * kBThreads;
       const int mm = a_k_fast ? i / kTK : i % kTM, kk = a_k_fast ? i % kTK : i / kTM;
       const int m = m0 + mm, k = k0 + kk;
-      as[kk][mm] = (m < M && k < K)
-                       ? ld_as_float(A, ab + (size_t)m * g.a_m + (size_t)k * g.a_k) : 0.f;
+      ra[r] = (m < M && k < K) ? ld_as_float(A, ab + (size_t)m * g.a_m + (size_t)k * g.a_k)
+                               : 0.f;
     }
-    for (int i = tid; i < kTN * kTK; i += kBThreads) {
+#pragma unroll
+    for (int r = 0; r < kRB; ++r) {
+      const int i = tid + r * kBThreads;
       const int nn = b_k_fast ? i / kTK : i % kTN, kk = b_k_fast ? i % kTK : i / kTN;
       const int n = n0 + nn, k = k0 + kk;
-      bs[kk][nn] = (n < N && k < K)
-                       ? ld_as_float(B, bb + (size_t)n * g.b_n + (size_t)k * g.b_k) : 0.f;
+      rb[r] = (n < N && k < K) ? ld_as_float(B, bb + (size_t)n * g.b_n + (size_t)k * g.b_k)
+                               : 0.f;
     }
+  };
+  auto stash = [&]() {
+#pragma unroll
+    for (int r = 0; r < kRA; ++r) {
+      const int i = tid + r * kBThreads;
+      const int mm = a_k_fast ? i / kTK : i % kTM, kk = a_k_fast ? i % kTK : i / kTM;
+      as[kk][mm] = ra[r];
+    }
+#pragma unroll
+    for (int r = 0; r < kRB; ++r) {
+      const int i = tid + r * kBThreads;
+      const int nn = b_k_fast ? i / kTK : i % kTN, kk = b_k_fast ? i % kTK : i / kTN;
+      bs[kk][nn] = rb[r];
+    }
+  };
+  if (K > 0) fetch(0);
+  for (int k0 = 0; k0 < K; k0 += kTK) {
+    stash();
     __syncthreads();
+    if (k0 + kTK < K) fetch(k0 + kTK);
 #pragma unroll
     for (int kk = 0; kk < kTK; ++kk) {
-      float av[4], bv[4];
+      const float4 a0 = *reinterpret_cast<const float4*>(&as[kk][ty * 8]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&as[kk][ty * 8 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&bs[kk][tx * 8]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&bs[kk][tx * 8 + 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) av[i] = as[kk][ty * 4 + i];
+      for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) bv[j] = bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
   const size_t cb = (size_t)b * g.c_b;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int m = m0 + ty * 8 + i;
     if (m >= M) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
+    for (int j = 0; j < 8; ++j) {
+      const int n = n0 + tx * 8 + j;
       if (n >= N) continue;
       float* c = g.C + cb + (size_t)m * g.c_m + (size_t)n * g.c_n;
       *c = g.accumulate ? *c + acc[i][j] : acc[i][j];
