@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -920,7 +921,8 @@ int switch_moe_route_expert_choice(const switch_moe_params* p, const float* logi
 namespace {
 
 struct BwdPlan {
-  size_t o_Xg, o_dO, o_O, o_dX, o_H, o_dH, o_L, o_dgate, o_tok, o_Hs, o_dHs, total;
+  size_t o_Xg, o_dO, o_O, o_dX, o_H, o_dH, o_L, o_dgate, o_tok, o_Hs, o_dHs, o_wgpart, total;
+  int wg_parts;   // token chunks of dW_g's reduction over the batch
 };
 
 int make_bwd_plan(const switch_moe_params* p, Plan* q, BwdPlan* b) {
@@ -941,6 +943,10 @@ int make_bwd_plan(const switch_moe_params* p, Plan* q, BwdPlan* b) {
   b->o_tok = take(NC * 4);
   b->o_Hs = q->shared ? take((size_t)q->T * q->F * 4) : 0;
   b->o_dHs = q->shared ? take((size_t)q->T * q->F * 4) : 0;
+  // dW_g reduces over all T tokens with only N x d outputs: its token range
+  // is cut into chunks of at least 256 (at most 32 chunks), summed in order
+  b->wg_parts = (int)std::min<int64_t>(32, std::max<int64_t>(1, q->T / 256));
+  b->o_wgpart = take((size_t)b->wg_parts * q->N * q->d * 4);
   b->total = o;
   return SWITCH_MOE_OK;
 }
@@ -1080,9 +1086,18 @@ int switch_moe_backward(const switch_moe_params* p, const void* x, const float* 
   if (!ok(launch_bgemm(g, x, bf, W_g, false, s)) || !ok(launch_bwd_router(a, s)))
     return SWITCH_MOE_ERR_CUDA;
   if (db_g && !ok(launch_bwd_colsum(a.L, db_g, T, N, s))) return SWITCH_MOE_ERR_CUDA;
-  g = bg(N, d, T, 1, dW_g);                               // dW_g = dl^T x over the tokens
-  g.a_m = 1; g.a_k = N; g.b_n = 1; g.b_k = d; g.c_m = d; g.c_n = 1;
-  if (!ok(launch_bgemm(g, a.L, false, x, bf, s))) return SWITCH_MOE_ERR_CUDA;
+  {                                                       // dW_g = dl^T x over the tokens
+    const int parts = bp.wg_parts, chunk = (T + parts - 1) / parts;
+    float* wgp = at<float>(ws, bp.o_wgpart);
+    g = bg(N, d, T, parts, wgp);
+    g.k_chunk = chunk;
+    g.a_b = (size_t)chunk * N; g.a_m = 1; g.a_k = N;
+    g.b_b = (size_t)chunk * d; g.b_n = 1; g.b_k = d;
+    g.c_b = (size_t)N * d; g.c_m = d; g.c_n = 1;
+    if (!ok(launch_bgemm(g, a.L, false, x, bf, s)) ||
+        !ok(launch_bwd_sum(wgp, parts, (size_t)N * d, dW_g, s)))
+      return SWITCH_MOE_ERR_CUDA;
+  }
   g = bg(T, d, N, 1, dx, true);                           // dx += dl W_g
   g.a_m = N; g.a_k = 1; g.b_n = 1; g.b_k = d; g.c_m = d; g.c_n = 1;
   if (!ok(launch_bgemm(g, a.L, false, W_g, false, s))) return SWITCH_MOE_ERR_CUDA;

@@ -21,6 +21,8 @@
 // recomputed from the inputs.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -49,7 +51,8 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemm_kernel(BGemmArgs g, const 
   const int b = blockIdx.z;
   const int M = g.mcount ? min(__ldg(g.mcount + b), g.M) : g.M;
   const int N = g.ncount ? min(__ldg(g.ncount + b), g.N) : g.N;
-  const int K = g.kcount ? min(__ldg(g.kcount + b), g.K) : g.K;
+  const int K = g.k_chunk ? min(g.k_chunk, g.K - b * g.k_chunk)
+                         : (g.kcount ? min(__ldg(g.kcount + b), g.K) : g.K);
   const int m0 = blockIdx.y * kTM, n0 = blockIdx.x * kTN;
   if (m0 >= M || n0 >= N) return;
   const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
@@ -242,7 +245,24 @@ __global__ void __launch_bounds__(256) bwd_colsum_kernel(const float* dl, float*
   if (threadIdx.x == 0) out[i] = sh[0];
 }
 
+__global__ void bwd_sum_kernel(const float* __restrict__ parts, int n_parts, size_t n,
+                               float* __restrict__ out) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int p = 0; p < n_parts; ++p) acc += parts[(size_t)p * n + i];
+    out[i] = acc;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_sum(const float* parts, int n_parts, size_t n, float* out,
+                           cudaStream_t s) {
+  const int grid = (int)std::min<size_t>((n + 255) / 256, 4 * 148);
+  bwd_sum_kernel<<<grid, 256, 0, s>>>(parts, n_parts, n, out);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bgemm(const BGemmArgs& g, const void* A, bool a_bf16, const void* B,
                          bool b_bf16, cudaStream_t s) {

@@ -417,6 +417,9 @@ struct BGemmArgs {
   size_t c_b, c_m, c_n;
   float* C;
   int accumulate;
+  // > 0: batch b takes the reduction range [b k_chunk, (b + 1) k_chunk) of K
+  // (its partial result goes to C + b c_b; launch_bwd_sum adds the parts)
+  int k_chunk;
 };
 cudaError_t launch_bgemm(const BGemmArgs& g, const void* A, bool a_bf16, const void* B,
                          bool b_bf16, cudaStream_t s);
@@ -448,6 +451,8 @@ cudaError_t launch_bwd_mask(float* dH, const float* H, const int32_t* counts, in
 cudaError_t launch_bwd_scatter(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_router(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_bwd_colsum(const float* dl, float* out, int T, int N, cudaStream_t s);
+// out[i] = sum_p parts[p n + i], parts in order (K-split partial results).
+cudaError_t launch_bwd_sum(const float* parts, int n_parts, size_t n, float* out, cudaStream_t s);
 
 // status word of the current device (see switch_moe_sync_status)
 int* device_status_ptr();
