@@ -64,26 +64,37 @@ __global__ void __launch_bounds__(kBThreads, 2) bgemm_kernel(BGemmArgs g, const 
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
   // the next K step's operands are loaded into registers while this one's
-  // FMAs run (one shared-memory stage, one register stage)
+  // FMAs run (one shared-memory stage, one register stage).  Each thread's
+  // element positions in the tile are fixed: their offsets are computed
+  // once, and a K step only adds k0 times the K stride.
   constexpr int kRA = kTM * kTK / kBThreads, kRB = kTN * kTK / kBThreads;
   float ra[kRA], rb[kRB];
+  size_t offa[kRA], offb[kRB];
+  int kka[kRA], kkb[kRB];
+#pragma unroll
+  for (int r = 0; r < kRA; ++r) {
+    const int i = tid + r * kBThreads;
+    const int mm = a_k_fast ? i / kTK : i % kTM;
+    kka[r] = a_k_fast ? i % kTK : i / kTM;
+    const bool ok = m0 + mm < M;
+    offa[r] = ok ? ab + (size_t)(m0 + mm) * g.a_m + (size_t)kka[r] * g.a_k : 0;
+    if (!ok) kka[r] = 1 << 30;   // never below K: the element reads as 0
+  }
+#pragma unroll
+  for (int r = 0; r < kRB; ++r) {
+    const int i = tid + r * kBThreads;
+    const int nn = b_k_fast ? i / kTK : i % kTN;
+    kkb[r] = b_k_fast ? i % kTK : i / kTN;
+    const bool ok = n0 + nn < N;
+    offb[r] = ok ? bb + (size_t)(n0 + nn) * g.b_n + (size_t)kkb[r] * g.b_k : 0;
+    if (!ok) kkb[r] = 1 << 30;
+  }
   auto fetch = [&](int k0) {
+    const size_t sa = (size_t)k0 * g.a_k, sb = (size_t)k0 * g.b_k;
 #pragma unroll
-    for (int r = 0; r < kRA; ++r) {
-      const int i = tid + r * kBThreads;
-      const int mm = a_k_fast ? i / kTK : i % kTM, kk = a_k_fast ? i % kTK : i / kTM;
-      const int m = m0 + mm, k = k0 + kk;
-      ra[r] = (m < M && k < K) ? ld_as_float(A, ab + (size_t)m * g.a_m + (size_t)k * g.a_k)
-                               : 0.f;
-    }
+    for (int r = 0; r < kRA; ++r) ra[r] = k0 + kka[r] < K ? ld_as_float(A, offa[r] + sa) : 0.f;
 #pragma unroll
-    for (int r = 0; r < kRB; ++r) {
-      const int i = tid + r * kBThreads;
-      const int nn = b_k_fast ? i / kTK : i % kTN, kk = b_k_fast ? i % kTK : i / kTN;
-      const int n = n0 + nn, k = k0 + kk;
-      rb[r] = (n < N && k < K) ? ld_as_float(B, bb + (size_t)n * g.b_n + (size_t)k * g.b_k)
-                               : 0.f;
-    }
+    for (int r = 0; r < kRB; ++r) rb[r] = k0 + kkb[r] < K ? ld_as_float(B, offb[r] + sb) : 0.f;
   };
   auto stash = [&]() {
 #pragma unroll
