@@ -14,6 +14,7 @@ Functions carry the C ABI's names:
     switch_moe_route_from_logits(logits, capacity_factor, ...) -> RouteOut
     switch_moe_forward_expert_choice(x, W_g, W1, W2, capacity_factor, ...) -> ExpertChoiceOut
     switch_moe_route_expert_choice(logits, capacity_factor) -> ExpertChoiceOut (y None)
+    switch_moe_backward(x, W_g, W1, W2, capacity_factor, fwd, dy, ...) -> BackwardOut
     switch_moe_router_logits(x, W_g, b_g=None) -> logits [T, N] fp32
     switch_moe_forward_hostio(x_host, W_g, W1, W2, ...) -> ForwardOut (host tensors)
     switch_moe_capacity(T, N, cf) -> int
